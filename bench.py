@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q4NX dequant-GEMV hot path on GB300: one JSON line.
+
+Workload (one "step"): a Qwen3-0.6B-shaped decode step at batch 1 -- 28 layers
+x 7 q4_1 projections (q 2048x1024, k/v 1024x1024, o 1024x2048, gate/up
+3072x1024, down 1024x3072), distinct seeded weights per (layer, matrix),
+275.25 MB of chunks, each matrix with its own bf16 N(0,1) activation vector.
+Every step streams all weights once (more than the 129 MB L2, so no step
+reuses L2-resident weights).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+value      = weight GB/s of the whole job (chunk bytes / s), inputs resident in HBM,
+             timed with CUDA events on the launching stream over exactly K steps
+             (CUDA-graph replays of the step), max over ranks.
+e2e        = the same metric through the public API with host buffers: per step
+             the activations go host->device from pinned memory, the step runs,
+             the outputs come back device->host, and the host synchronises.
+roofline   = the dominant kernel (q4nx GEMV): algorithmic bytes per launch
+             (chunks + x + y) / mean launch duration, against the measured HBM
+             copy bandwidth.
+cpu_baseline / --impl reference = the oracle (plain C, binary64, one core)
+             on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Q4NX fused dequant-GEMV weight GB/s (% of HBM peak); M=64 GEMM TFLOPS"
+WORKLOAD = "Qwen3-0.6B-shaped decode layer x28, q4_1, batch 1"
+WORKLOAD_ID = 2
+CHUNK = synth.CHUNK_BYTES[synth.Q4_1]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _matrices():
+    """(layer, matrix_id, N, K) of one step."""
+    return [(l, mi, n, k) for l in range(synth.QWEN3_06B_LAYERS) for mi, (_, n, k) in enumerate(synth.QWEN3_06B_LAYER)]
+
+
+def _gen(layer, mi, N, K):
+    f, w = synth.workload_weight(WORKLOAD_ID, mi, layer=layer, shape=(N, K))
+    x = synth.workload_activations(WORKLOAD_ID, mi, 1, K, layer=layer)[0]
+    return w, x
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- CPU arms --
+
+def cpu_oracle_sample(mats, gen, budget_s: float, start: int = 0):
+    """Run the oracle over matrices of the workload until `budget_s` is spent.
+    Returns (weight bytes, seconds, matrices done)."""
+    import oracle
+
+    done, nbytes, t_used = 0, 0, 0.0
+    i = start
+    while t_used < budget_s and done < len(mats):
+        l, mi, N, K = mats[i % len(mats)]
+        w, x = gen(l, mi, N, K)
+        t0 = time.perf_counter()
+        oracle.matmul(w, oracle.Q4_1, N, K, x)
+        t_used += time.perf_counter() - t0
+        nbytes += w.size
+        done += 1
+        i += 1
+    return nbytes, t_used, done
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    mats = _matrices()
+    steps, warm = args.steps, args.warmup
+    per_step = max(0.02, min(10.0, 150.0 / (steps + warm)))
+    for s in range(warm):
+        cpu_oracle_sample(mats, _gen, per_step, start=s)
+    tot_b, tot_t, tot_m = 0, 0.0, 0
+    for s in range(steps):
+        b, t, m = cpu_oracle_sample(mats, _gen, per_step, start=warm + s)
+        tot_b += b
+        tot_t += t
+        tot_m += m
+    gbs = tot_b / tot_t / 1e9
+    sample = (f"oracle binary64 matvec (plain C, 1 thread) over {tot_m} matrices of the workload "
+              f"(~{per_step:.2f} s per step, {tot_b / 1e6:.1f} MB of chunks)")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": "bounded per step"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+def run_gpu(args, rank: int, world: int):
+    import torch
+
+    import dequant_gemv_gb300 as q
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mats = _matrices()
+
+    # inputs: all weights in one device buffer, all x in one, all y in one
+    offs, xoffs, yoffs = [], [], []
+    wtot = xtot = ytot = 0
+    for (_, _, N, K) in mats:
+        offs.append(wtot)
+        xoffs.append(xtot)
+        yoffs.append(ytot)
+        wtot += (N // 32) * (K // 256) * CHUNK
+        xtot += K
+        ytot += N
+    wdev = torch.empty(wtot, dtype=torch.uint8, device=dev)
+    x_host = torch.empty(xtot, dtype=torch.bfloat16, pin_memory=True)
+    for i, (l, mi, N, K) in enumerate(mats):
+        w, x = _gen(l, mi, N, K)
+        wdev[offs[i]:offs[i] + w.size].copy_(torch.from_numpy(w))
+        x_host[xoffs[i]:xoffs[i] + K].copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+    xdev = x_host.to(dev)
+    ydev = torch.empty(ytot, dtype=torch.bfloat16, device=dev)
+    y_host = torch.empty(ytot, dtype=torch.bfloat16, pin_memory=True)
+    weights = [q.Weight(wdev[offs[i]:offs[i] + (N // 32) * (K // 256) * CHUNK], q.Q4NX_Q4_1, N, K)
+               for i, (_, _, N, K) in enumerate(mats)]
+    xs = [xdev[xoffs[i]:xoffs[i] + K] for i, (_, _, N, K) in enumerate(mats)]
+    ys = [ydev[yoffs[i]:yoffs[i] + N] for i, (_, _, N, K) in enumerate(mats)]
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        items = [(weights[i], xs[i], ys[i]) for i in range(len(mats))]
+        ws_need = int(q.lib.q4nx_gemv_batch_workspace((q.q4nx_gemv_item * len(items))(
+            *[q.q4nx_gemv_item(W.c(), x.data_ptr(), y.data_ptr()) for W, x, y in items]), len(items)))
+        ws = torch.zeros(max(ws_need, 1 << 20), dtype=torch.uint8, device=dev)
+        # the step: every matrix of the 28 layers in one batched launch
+        step_batch = q.GemvBatch(items, "bf16", ws)
+        # the same work respecting a decode layer's data dependencies: {q,k,v}, {o}, {gate,up}, {down}
+        per_layer = []
+        for l in range(synth.QWEN3_06B_LAYERS):
+            base = 7 * l
+            for grp in ((0, 1, 2), (3,), (4, 5), (6,)):
+                per_layer.append(q.GemvBatch([items[base + j] for j in grp], "bf16", ws))
+    torch.cuda.synchronize()
+
+    def capture(fn):
+        with torch.cuda.stream(stream):
+            fn()                                     # eager run once (kernel attributes)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    graph = capture(step_batch)
+    launches_per_step = 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    gpu_uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    clocks = ClockSampler(gpu_uuid)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)                              # let the sampler start before the timed region
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * wtot * args.steps / (ms / 1e3) / 1e9
+
+    # other schedules of the same step, for context (not the headline)
+    def time_graph(g, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            a.record(stream)
+            for _ in range(n):
+                g.replay()
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / n
+    alt = {}
+    if not args.no_alt:
+        g_layer = capture(lambda: [b() for b in per_layer])
+        alt["per_layer_4_launches_gbs"] = wtot / (time_graph(g_layer, 200) / 1e3) / 1e9
+        g_single = capture(lambda: [q.q4nx_gemv(weights[i], xs[i], out=ys[i], ws=ws) for i in range(len(mats))])
+        alt["one_launch_per_matrix_gbs"] = wtot / (time_graph(g_single, 100) / 1e3) / 1e9
+        del g_layer, g_single
+
+    # roofline of the dominant kernel (every launch of the step is the GEMV)
+    alg_bytes_step = wtot + 2 * xtot + 2 * ytot
+    launch_us = ms_per_step * 1e3 / launches_per_step
+    achieved = alg_bytes_step / launches_per_step / (launch_us * 1e-6) / 1e9
+    peak, peak_kind = _peaks()
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get("gemv_q4_1_bytes_per_launch")
+
+    # end to end through the public API with host buffers
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            xdev.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(ydev, non_blocking=True)
+            stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            xdev.copy_(x_host, non_blocking=True)
+            graph.replay()
+            y_host.copy_(ydev, non_blocking=True)
+            stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_e2e = float(t.item())
+    e2e_value = world * wtot * e2e_steps / t_e2e / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        b, t, m = cpu_oracle_sample(mats, _gen, args.cpu_seconds)
+        cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"oracle binary64 matvec (plain C, 1 thread) over the first {m} of the step's "
+                         f"{len(mats)} matrices ({b / 1e6:.1f} MB of chunks, {t:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": synth.QWEN3_06B_LAYERS, "matrices_per_step": len(mats),
+                       "weight_bytes_per_step": wtot, "kind": "q4_1", "batch": 1,
+                       "l2": "inputs larger than L2 (275 MB of weights streamed per step)",
+                       "launch": "one q4nx_gemv_batch launch of all 196 matrices per step, CUDA-graph replay",
+                       "other_schedules": alt,
+                       "hbm_frac_of_nominal_8tbs": value / 8000.0},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                         "bytes_per_launch": alg_bytes_step / launches_per_step,
+                         "launch_us": launch_us},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * xtot,
+                    "d2h_bytes_per_step": 2 * ytot},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

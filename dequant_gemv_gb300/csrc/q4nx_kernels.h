@@ -1,0 +1,61 @@
+// q4nx_kernels.h -- host-side launchers of the Q4NX kernels (internal to libq4nx.so).
+// The C ABI in include/q4nx.h validates arguments and then calls these.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q4nx {
+
+struct DeviceInfo {
+  int sms = 0;
+  int max_smem_optin = 0;
+};
+// Properties of the current device (cached per device ordinal).
+cudaError_t device_info(DeviceInfo* out);
+
+// Raise a kernel's dynamic shared-memory limit to the device maximum once per
+// (device, slot); slots 0..31.
+cudaError_t set_max_dynamic_smem(const void* func, int slot);
+
+// ---- GEMV (M = 1), a batch of independent items of one kind per launch ----
+constexpr int kMaxGemvItems = 256;
+struct GemvItem {
+  const void* chunks;
+  const void* x;
+  void* y;
+  int64_t TR, TC;
+};
+struct GemvPlan {
+  int warps = 0;       // warp workers per CTA
+  int stages = 0;      // ring stages per warp
+  int grid = 0;        // CTAs
+  int workers = 0;     // warp workers in the grid, <= chunks
+  size_t smem = 0;     // dynamic shared memory bytes
+};
+bool gemv_plan(int kind, int64_t total_chunks, int sms, int max_smem, GemvPlan* plan);
+uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks);
+cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
+                              int max_smem, cudaStream_t s);
+
+// ---- standalone decode ----
+cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s);
+
+// ---- Q4_K -> q4_1 repack ----
+cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out, cudaStream_t s);
+
+// ---- top-1 ----
+cudaError_t launch_argmax(const float* logits, int M, int64_t V, int32_t* idx, cudaStream_t s);
+
+// ---- GEMM (M <= 64, tcgen05) ----
+bool gemm_available();
+uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M);
+cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, const void* X, int M, void* Y,
+                        int out_f32, void* workspace, cudaStream_t s);
+
+// Workspace layout shared by the GEMV launcher and kernel.
+constexpr uint64_t kWsErrBytes = 16;              // error word (+ padding)
+constexpr int kMaxWorkers = 4096;                 // upper bound of warp workers per launch
+__host__ __device__ inline uint64_t align16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
+
+}  // namespace q4nx

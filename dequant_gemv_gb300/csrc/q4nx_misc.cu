@@ -1,0 +1,224 @@
+// q4nx_misc.cu -- standalone decode, Q4_K -> q4_1 repack and top-1 kernels.
+//
+// Formulas: the "Q4NX chunks" section of the 1bit engine "NPU engine" page
+// (chunk-kind table; the decoders-and-repack paragraph below it).  Greedy
+// top-1: the page's "Serving" section (greedy decoding).
+#include <cooperative_groups.h>
+
+#include "q4nx_device.cuh"
+#include "q4nx_kernels.h"
+
+namespace cg = cooperative_groups;
+
+namespace q4nx {
+
+// ------------------------------------------------------------- decode ----
+//
+// Every weight is formed in binary32 one operation at a time and rounded to
+// bf16 nearest-even:  q4_1 (c*s)+z;  Q4_K ((S*sc)*c)+(M*mn);  Q8 d*c.
+// The products are exact in binary32; __fmul_rn/__fadd_rn keep the compiler
+// from contracting them into an FMA.
+
+// 4-bit kinds: one CTA of 256 threads per chunk; warp w handles rows
+// 4w..4w+3, lane L the 8 columns 8L..8L+7 (one 32-bit code word), and each
+// row of 256 outputs is one coalesced 512-byte store.
+template <int KIND>
+__global__ void __launch_bounds__(256) decode_q4_kernel(const uint8_t* __restrict__ chunks, int64_t TC,
+                                                        uint16_t* __restrict__ out) {
+  constexpr int CB = chunk_bytes_of(KIND);
+  const int64_t t = blockIdx.x;
+  const int64_t tr = t / TC, tc = t - tr * TC;
+  const int64_t K = TC * 256;
+  const uint8_t* ch = chunks + t * CB;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = warp * 4 + j;
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(ch + r * 128) + lane);
+    float s, z, S = 0.f, M = 0.f, sc = 0.f, mn = 0.f;
+    if constexpr (KIND == kQ4_1) {
+      s = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(ch + kQ41Scale) + r * 8 + g));
+      z = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(ch + kQ41Zero) + r * 8 + g));
+    } else {
+      S = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(ch + kQ4KS) + r));
+      M = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(ch + kQ4KM) + r));
+      sc = static_cast<float>(__ldg(ch + kQ4KSc + r * 8 + g));
+      mn = static_cast<float>(__ldg(ch + kQ4KMn + r * 8 + g));
+      s = __fmul_rn(S, sc);      // exact
+      z = __fmul_rn(M, mn);      // exact
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float c0 = static_cast<float>((w >> (8 * p)) & 0xF);
+      const float c1 = static_cast<float>((w >> (8 * p + 4)) & 0xF);
+      const float w0 = __fadd_rn(__fmul_rn(c0, s), z);
+      const float w1 = __fadd_rn(__fmul_rn(c1, s), z);
+      o[p] = static_cast<uint32_t>(f32_to_bf16_bits(w0)) | (static_cast<uint32_t>(f32_to_bf16_bits(w1)) << 16);
+    }
+    uint16_t* dst = out + (tr * 32 + r) * K + tc * 256 + lane * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Q8 kinds: the chunk's codes are column-oriented, so the CTA stages them in
+// shared memory; lane = row, and each thread emits 8 consecutive columns.
+template <int KIND>
+__global__ void __launch_bounds__(256) decode_q8_kernel(const uint8_t* __restrict__ chunks, int64_t TC,
+                                                        uint16_t* __restrict__ out) {
+  __shared__ __align__(16) uint8_t sc[kQ8Bytes];
+  const int64_t t = blockIdx.x;
+  const int64_t tr = t / TC, tc = t - tr * TC;
+  const int64_t K = TC * 256;
+  const uint4* src = reinterpret_cast<const uint4*>(chunks + t * kQ8Bytes);
+  for (int i = threadIdx.x; i < kQ8Bytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(sc)[i] = __ldg(src + i);
+  __syncthreads();
+  const int r = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = warp + 8 * jj;           // 8-column block 0..31
+    const int gidx = j >> 2;
+    const float d = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(sc + kQ8D)[r * 8 + gidx]);
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      float wv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int k = 8 * j + 2 * p + e;
+        int off;
+        if constexpr (KIND == kQ8_KR) off = k * 32 + r;
+        else off = (r >> 4) * 4096 + (k >> 5) * 512 + (k & 31) * 16 + (r & 15);
+        wv[e] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc[off])));
+      }
+      o[p] = static_cast<uint32_t>(f32_to_bf16_bits(wv[0])) | (static_cast<uint32_t>(f32_to_bf16_bits(wv[1])) << 16);
+    }
+    uint16_t* dst = out + (tr * 32 + r) * K + tc * 256 + j * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s) {
+  const int64_t T = TR * TC;
+  const uint8_t* c = static_cast<const uint8_t*>(chunks);
+  uint16_t* o = static_cast<uint16_t*>(out);
+  if (T > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(T));
+  switch (kind) {
+    case kQ4_1: decode_q4_kernel<kQ4_1><<<grid, 256, 0, s>>>(c, TC, o); break;
+    case kQ4_K: decode_q4_kernel<kQ4_K><<<grid, 256, 0, s>>>(c, TC, o); break;
+    case kQ8_KR: decode_q8_kernel<kQ8_KR><<<grid, 256, 0, s>>>(c, TC, o); break;
+    case kQ8_BLK: decode_q8_kernel<kQ8_BLK><<<grid, 256, 0, s>>>(c, TC, o); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- repack ----
+//
+// Q4_K chunk -> q4_1 chunk: the 4096 code bytes are copied unchanged;
+// scale = bf16(S*sc), zero = bf16(M*mn) per (row, group).  S*sc and M*mn are
+// exact binary32 products (8 x 8 significant bits), so the bf16 rounding is
+// the only rounding.  One CTA of 256 threads per chunk.
+__global__ void __launch_bounds__(256) repack_q4k_kernel(const uint8_t* __restrict__ in, uint8_t* __restrict__ out) {
+  const int64_t t = blockIdx.x;
+  const uint8_t* src = in + t * kQ4KBytes;
+  uint8_t* dst = out + t * kQ41Bytes;
+  const int i = threadIdx.x;                          // 256 threads: 16 B of codes each
+  reinterpret_cast<uint4*>(dst)[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+  const int r = i >> 3;                               // (row, group) pair i = r*8 + g
+  const float S = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(src + kQ4KS) + r));
+  const float M = bf16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(src + kQ4KM) + r));
+  const float sc = static_cast<float>(__ldg(src + kQ4KSc + i));
+  const float mn = static_cast<float>(__ldg(src + kQ4KMn + i));
+  reinterpret_cast<uint16_t*>(dst + kQ41Scale)[i] = f32_to_bf16_bits(__fmul_rn(S, sc));
+  reinterpret_cast<uint16_t*>(dst + kQ41Zero)[i] = f32_to_bf16_bits(__fmul_rn(M, mn));
+}
+
+cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out, cudaStream_t s) {
+  const int64_t T = TR * TC;
+  if (T > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  repack_q4k_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(static_cast<const uint8_t*>(in),
+                                                              static_cast<uint8_t*>(out));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- argmax ----
+//
+// Each (value, index) becomes a 64-bit key whose unsigned order is the
+// wanted order: NaN above +inf above every number, +0 == -0, and for equal
+// values the lower index above.  A cluster of 8 CTAs reduces one row: each
+// CTA scans an eighth, then CTA 0 reads the others' maxima through
+// distributed shared memory.  No workspace, no atomics, deterministic.
+constexpr int kArgmaxCluster = 8;
+constexpr int kArgmaxThreads = 256;
+
+__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
+  uint32_t ord;
+  if (v != v) {
+    ord = 0xFFFFFFFFu;
+  } else {
+    uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+    ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(~idx);
+}
+
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
+    argmax_kernel(const float* __restrict__ logits, int64_t V, int32_t* __restrict__ idx) {
+  __shared__ uint64_t warp_best[kArgmaxThreads / 32];
+  __shared__ uint64_t cta_best;
+  cg::cluster_group cluster = cg::this_cluster();
+  const unsigned rank = cluster.block_rank();
+  const int64_t m = blockIdx.y;
+  const float* row = logits + m * V;
+  const int64_t per = (V + kArgmaxCluster - 1) / kArgmaxCluster;
+  const int64_t b0 = rank * per;
+  const int64_t b1 = (b0 + per < V) ? b0 + per : V;
+  uint64_t best = 0;
+  const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15) == 0) && ((b0 & 3) == 0);
+  if (vec && b1 > b0) {
+    const int64_t n4 = (b1 - b0) / 4;
+    const float4* r4 = reinterpret_cast<const float4*>(row + b0);
+    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+      const float4 v = __ldg(r4 + i);
+      const uint32_t k = static_cast<uint32_t>(b0 + 4 * i);
+      best = umax64(best, argmax_key(v.x, k));
+      best = umax64(best, argmax_key(v.y, k + 1));
+      best = umax64(best, argmax_key(v.z, k + 2));
+      best = umax64(best, argmax_key(v.w, k + 3));
+    }
+    for (int64_t i = b0 + 4 * n4 + threadIdx.x; i < b1; i += blockDim.x)
+      best = umax64(best, argmax_key(__ldg(row + i), static_cast<uint32_t>(i)));
+  } else {
+    for (int64_t i = b0 + threadIdx.x; i < b1; i += blockDim.x)
+      best = umax64(best, argmax_key(__ldg(row + i), static_cast<uint32_t>(i)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if ((threadIdx.x & 31) == 0) warp_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t b = 0;
+    for (int w = 0; w < kArgmaxThreads / 32; ++w) b = umax64(b, warp_best[w]);
+    cta_best = b;
+  }
+  cluster.sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    uint64_t b = 0;
+    for (unsigned r = 0; r < kArgmaxCluster; ++r) b = umax64(b, *cluster.map_shared_rank(&cta_best, r));
+    idx[m] = static_cast<int32_t>(~static_cast<uint32_t>(b & 0xFFFFFFFFu));
+  }
+  cluster.sync();      // peers keep their shared memory until rank 0 has read it
+}
+
+cudaError_t launch_argmax(const float* logits, int M, int64_t V, int32_t* idx, cudaStream_t s) {
+  const dim3 grid(kArgmaxCluster, static_cast<unsigned>(M));
+  argmax_kernel<<<grid, kArgmaxThreads, 0, s>>>(logits, V, idx);
+  return cudaGetLastError();
+}
+
+}  // namespace q4nx

@@ -1,0 +1,162 @@
+/*
+ * q4nx.h -- C ABI of libq4nx.so: Q4NX dequant-GEMV / GEMM on one GB300 (sm_103a).
+ *
+ * Operations come from the 1bit engine page "NPU engine" (docs/npu.md),
+ * section "Q4NX chunks": a weight W[N][K] is a grid of 32-row x 256-column
+ * tiles, one chunk per tile, chunks row-major over the grid; three chunk kinds
+ * (chunk-kind table), two Q8 code layouts, decoders for all kinds, and the
+ * Q4_K -> q4_1 repack.
+ *
+ * Byte order inside a chunk (the page does not print it; this library fixes it):
+ *   q4_1  5120 B: codes 4096 | scale bf16 [32 r][8 g] | zero bf16 [32 r][8 g]
+ *   Q4_K  4736 B: codes 4096 | sc u8 [32][8] | mn u8 [32][8] | S bf16 [32] | M bf16 [32]
+ *   Q8    8704 B: codes int8 8192 (layout KR or BLK) | d bf16 [32 r][8 g]
+ *   4-bit code (r, k): byte r*128 + k/2, low nibble for even k, high for odd k.
+ *   g = k/32.  All bf16 fields little-endian.
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_dev are device pointers (cudaMalloc'd or from a
+ *     framework allocator); the caller owns them.  The library allocates
+ *     nothing, frees nothing and keeps no pointer after a call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it; nothing synchronises.
+ *   - Arguments are validated before anything is enqueued.  A non-zero status
+ *     means nothing was launched and no output byte was written, except
+ *     Q4NX_E_CUDA (the launch itself failed; outputs undefined).
+ *   - Device buffers must start on 16-byte boundaries (Q4NX_E_ALIGN).
+ *   - No exception crosses this boundary; there is no global error state.
+ *   - Calls are thread-safe.  Two calls that share a workspace must not
+ *     overlap on the GPU.
+ */
+#ifndef Q4NX_H
+#define Q4NX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Chunk kinds ("Q4NX chunks", chunk-kind table; Q8 layouts from the paragraph below it). */
+enum q4nx_kind {
+    Q4NX_Q4_1 = 1,    /* 5120 B: w = code*scale + zero                               */
+    Q4NX_Q4_K = 2,    /* 4736 B: w = S*sc*code + M*mn                                */
+    Q4NX_Q8_KR = 3,   /* 8704 B: w = d*code, code (r,k) at byte k*32 + r             */
+    Q4NX_Q8_BLK = 4   /* 8704 B: code (r,k) at (r/16)*4096+(k/32)*512+(k%32)*16+r%16 */
+};
+
+/* Status codes. */
+enum q4nx_status {
+    Q4NX_OK = 0,
+    Q4NX_E_NULL = 1,            /* a required pointer is NULL                          */
+    Q4NX_E_KIND = 2,            /* unknown chunk kind                                  */
+    Q4NX_E_SHAPE = 3,           /* rows % 32, cols % 256, or a size <= 0               */
+    Q4NX_E_SHORT = 4,           /* a buffer is shorter than its layout needs           */
+    Q4NX_E_ALIGN = 5,           /* a device buffer is not 16-byte aligned              */
+    Q4NX_E_M = 6,               /* M outside 1..64                                     */
+    Q4NX_E_WORKSPACE = 7,       /* workspace NULL or smaller than the *_workspace size */
+    Q4NX_E_UNSUPPORTED = 8,     /* valid kind, but not for this operation / size       */
+    Q4NX_E_CUDA = 9,            /* a CUDA call failed (launch error)                   */
+    Q4NX_E_DEVICE_TIMEOUT = 10, /* a bounded in-kernel wait gave up (see q4nx_check)   */
+    Q4NX_E_DTYPE = 11           /* unknown output dtype                                */
+};
+
+/* Output element type of the products. */
+enum q4nx_out { Q4NX_OUT_BF16 = 0, Q4NX_OUT_F32 = 1 };
+
+/* A Q4NX weight: `rows` x `cols` (N x K), TR = rows/32 tile rows by TC = cols/256
+ * tile columns, chunk (tr, tc) at byte (tr*TC + tc) * chunk_bytes(kind).
+ * A contiguous range of tile rows of a larger weight is itself a weight
+ * (chunks_dev advanced by tr0*TC*chunk_bytes, rows = count*32). */
+typedef struct q4nx_weight {
+    const void* chunks_dev;   /* device, 16-byte aligned                          */
+    uint64_t bytes;           /* length of the chunk buffer                       */
+    int32_t kind;             /* enum q4nx_kind                                   */
+    int32_t reserved;         /* must be 0                                        */
+    int64_t rows;             /* N, multiple of 32                                */
+    int64_t cols;             /* K, multiple of 256                               */
+} q4nx_weight;
+
+/* Bytes of one chunk of `kind` (5120, 4736, 8704, 8704), 0 for an unknown kind. */
+uint64_t q4nx_chunk_bytes(int kind);
+
+/* A static, human-readable name of a status code. */
+const char* q4nx_status_str(int status);
+
+/* Library ABI version (bumped on any signature change). */
+int q4nx_abi_version(void);
+
+/* Decode a whole weight to bf16 ("Q4NX chunks", decoders paragraph).
+ * out_dev: bf16 [rows][cols] row-major, rows*cols*2 bytes.
+ * Each weight is formed in binary32 one operation at a time (no contraction):
+ *   q4_1 (code*scale) + zero;  Q4_K ((S*sc)*code) + (M*mn);  Q8 d*code,
+ * then rounded to bf16 to nearest-even.  Every product is exact in binary32,
+ * so the result is bf16(fl32(exact)).  All four kinds. */
+int q4nx_decode(const q4nx_weight* w, void* out_dev, uint64_t out_bytes, void* stream);
+
+/* Fused decode + GEMV, one token:  y[n] = sum_k w[n][k] * x[k]  (fp32 accumulation).
+ * x_dev: bf16 [cols].  y_dev: [rows] of out_dtype (bf16 rounds to nearest-even;
+ * fp32 is meant for lm_head logits).  All four kinds, any cols.
+ * workspace_dev: device scratch of at least q4nx_gemv_workspace(w) bytes, 16-byte
+ * aligned, ZERO-FILLED before its first use; every call leaves it zero-filled
+ * again (after Q4NX_E_DEVICE_TIMEOUT it must be zero-filled anew).  It holds
+ * split-K partial sums, per-tile-row arrival counters and an error word.
+ * Results are deterministic: partials are added in a fixed order. */
+int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype,
+              void* workspace_dev, uint64_t workspace_bytes, void* stream);
+uint64_t q4nx_gemv_workspace(const q4nx_weight* w);
+
+/* One GEMV of a batch: y_dev[rows] = w * x_dev[cols]. */
+typedef struct q4nx_gemv_item {
+    q4nx_weight w;
+    const void* x_dev;        /* bf16 [w.cols], 16-byte aligned */
+    void* y_dev;              /* [w.rows] of the batch's out_dtype, 16-byte aligned */
+} q4nx_gemv_item;
+
+/* Up to Q4NX_MAX_BATCH independent GEMVs of ONE chunk kind in one launch: the
+ * chunks of all items are spread evenly over the GPU, so many small matrices
+ * (a decode layer's projections) stream at the bandwidth of one large one.
+ * `items` is a HOST array (read during the call only).  Each item behaves as
+ * q4nx_gemv; the workspace is q4nx_gemv_batch_workspace(items, count) bytes
+ * under the same zero-fill rule.  Q4NX_E_KIND if the kinds differ,
+ * Q4NX_E_SHAPE if count is outside 1..Q4NX_MAX_BATCH. */
+#define Q4NX_MAX_BATCH 256
+int q4nx_gemv_batch(const q4nx_gemv_item* items, int count, int out_dtype,
+                    void* workspace_dev, uint64_t workspace_bytes, void* stream);
+uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
+
+/* Fused decode + GEMM for a block of 1..64 tokens on the tcgen05 tensor cores:
+ *   Y[m][n] = sum_k X[m][k] * w[n][k],  m < M.
+ * X_dev: bf16 [M][cols] row-major.  Y_dev: [M][rows] row-major of out_dtype.
+ * Weights are decoded to bf16 in the kernel (bit-identical to q4nx_decode) and
+ * multiplied with fp32 accumulation.  Kinds: q4_1, Q8_KR, Q8_BLK; Q4_K returns
+ * Q4NX_E_UNSUPPORTED (repack it with q4nx_repack_q4k first).
+ * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes, zero-filled before
+ * first use (it holds the error word). */
+int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, int out_dtype,
+                  void* workspace_dev, uint64_t workspace_bytes, void* stream);
+uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M);
+
+/* Q4_K -> q4_1 repack ("Q4NX chunks", decoders paragraph): codes copied byte for
+ * byte; scale = bf16(S*sc), zero = bf16(M*mn) per (row, group), nearest-even.
+ * in_dev: TR*TC Q4_K chunks (in_bytes >= TR*TC*4736).  out_dev: TR*TC q4_1
+ * chunks (out_bytes >= TR*TC*5120).  rows, cols as for a weight. */
+int q4nx_repack_q4k(const void* in_dev, uint64_t in_bytes, int64_t rows, int64_t cols,
+                    void* out_dev, uint64_t out_bytes, void* stream);
+
+/* Top-1 of each row of fp32 logits [M][V] (greedy decoding, "Serving" section):
+ * idx_dev[m] = index of the first maximum; a NaN counts above every number and
+ * the first NaN wins; +0 and -0 are equal.  1 <= M <= 65535, 1 <= V < 2^31. */
+int q4nx_argmax(const float* logits_dev, int M, int64_t V, int32_t* idx_dev, void* stream);
+
+/* Read and clear the error word of a workspace (synchronises `stream`).
+ * Returns Q4NX_OK, or Q4NX_E_DEVICE_TIMEOUT if a bounded in-kernel wait of a
+ * call that used this workspace gave up (its outputs are then invalid). */
+int q4nx_check(void* workspace_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4NX_H */

@@ -1,0 +1,133 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+libq4nx.so loads, exports every function include/q4nx.h declares, and
+rejects bad arguments with the documented status before touching the GPU
+(the "Q4NX chunks" section of the 1bit engine "NPU engine" page: refuse an
+unknown chunk size or a tensor shorter than its layout needs).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q():
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build()
+    import dequant_gemv_gb300
+
+    return dequant_gemv_gb300
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "q4nx.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4nx_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(q):
+    names = _declared()
+    assert "q4nx_gemv" in names and "q4nx_gemm_m64" in names and len(names) >= 11
+    lib = ctypes.CDLL(q.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(q.EXPORTS)
+
+
+def test_chunk_bytes_and_strings(q):
+    assert [q.q4nx_chunk_bytes(k) for k in (1, 2, 3, 4)] == [5120, 4736, 8704, 8704]
+    assert q.q4nx_chunk_bytes(0) == 0 and q.q4nx_chunk_bytes(9) == 0
+    assert q.lib.q4nx_abi_version() == 1
+    for s in range(0, 12):
+        assert q.q4nx_status_str(s) != "unknown status"
+    assert q.q4nx_status_str(99) == "unknown status"
+
+
+def _w(q, ptr=16, nbytes=5120, kind=1, rows=32, cols=256, reserved=0):
+    return q.q4nx_weight(ptr, nbytes, kind, reserved, rows, cols)
+
+
+def test_validation_statuses(q):
+    L = q.lib
+    by = ctypes.byref
+    P = 0x10000                      # a fake, 16-byte aligned "device" address: never dereferenced
+    # decode
+    assert L.q4nx_decode(None, P, 1 << 20, None) == 1
+    assert L.q4nx_decode(by(_w(q, ptr=None)), P, 1 << 20, None) == 1
+    assert L.q4nx_decode(by(_w(q, ptr=P, kind=7)), P, 1 << 20, None) == 2
+    assert L.q4nx_decode(by(_w(q, ptr=P, reserved=1)), P, 1 << 20, None) == 2
+    assert L.q4nx_decode(by(_w(q, ptr=P, rows=31)), P, 1 << 20, None) == 3
+    assert L.q4nx_decode(by(_w(q, ptr=P, cols=255)), P, 1 << 20, None) == 3
+    assert L.q4nx_decode(by(_w(q, ptr=P, rows=0)), P, 1 << 20, None) == 3
+    assert L.q4nx_decode(by(_w(q, ptr=P, rows=-32)), P, 1 << 20, None) == 3
+    assert L.q4nx_decode(by(_w(q, ptr=P, nbytes=5119)), P, 1 << 20, None) == 4
+    assert L.q4nx_decode(by(_w(q, ptr=P, kind=3, nbytes=5120)), P, 1 << 20, None) == 4
+    assert L.q4nx_decode(by(_w(q, ptr=P + 8)), P, 1 << 20, None) == 5
+    assert L.q4nx_decode(by(_w(q, ptr=P)), None, 1 << 20, None) == 1
+    assert L.q4nx_decode(by(_w(q, ptr=P)), P, 32 * 256 * 2 - 1, None) == 4
+    assert L.q4nx_decode(by(_w(q, ptr=P)), P + 4, 1 << 20, None) == 5
+    # gemv
+    w = _w(q, ptr=P)
+    need = L.q4nx_gemv_workspace(by(w))
+    assert need >= 16
+    assert L.q4nx_gemv(by(w), None, P, 0, P, need, None) == 1
+    assert L.q4nx_gemv(by(w), P, P, 2, P, need, None) == 11
+    assert L.q4nx_gemv(by(w), P, P, 0, None, need, None) == 7
+    assert L.q4nx_gemv(by(w), P, P, 0, P, need - 1, None) == 7
+    assert L.q4nx_gemv(by(w), P + 2, P, 0, P, need, None) == 5
+    assert L.q4nx_gemv_workspace(by(_w(q, rows=33))) == 0
+    # gemv batch
+    items = (q.q4nx_gemv_item * 3)()
+    for i in range(3):
+        items[i].w = _w(q, ptr=P, rows=64, cols=512, nbytes=4 * 5120)
+        items[i].x_dev = P
+        items[i].y_dev = P
+    bneed = L.q4nx_gemv_batch_workspace(items, 3)
+    assert bneed >= L.q4nx_gemv_workspace(by(items[0].w))
+    assert L.q4nx_gemv_batch_workspace(items, 0) == 0
+    assert L.q4nx_gemv_batch(None, 3, 0, P, bneed, None) == 1
+    assert L.q4nx_gemv_batch(items, 0, 0, P, bneed, None) == 3
+    assert L.q4nx_gemv_batch(items, 257, 0, P, bneed, None) == 3
+    assert L.q4nx_gemv_batch(items, 3, 0, P, bneed - 1, None) == 7
+    items[2].w = _w(q, ptr=P, kind=2, rows=64, cols=512, nbytes=4 * 4736)
+    assert L.q4nx_gemv_batch(items, 3, 0, P, bneed, None) == 2
+    items[2].w = _w(q, ptr=P, rows=64, cols=512, nbytes=4 * 5120 - 1)
+    assert L.q4nx_gemv_batch(items, 3, 0, P, bneed, None) == 4
+    items[2].w = _w(q, ptr=P, rows=64, cols=512, nbytes=4 * 5120)
+    items[1].y_dev = P + 2
+    assert L.q4nx_gemv_batch(items, 3, 0, P, bneed, None) == 5
+    # gemm
+    gneed = L.q4nx_gemm_workspace(by(w), 64)
+    assert L.q4nx_gemm_workspace(by(w), 0) == 0 and L.q4nx_gemm_workspace(by(w), 65) == 0
+    assert L.q4nx_gemm_m64(by(w), P, 0, P, 0, P, gneed, None) == 6
+    assert L.q4nx_gemm_m64(by(w), P, 65, P, 0, P, gneed, None) == 6
+    assert L.q4nx_gemm_m64(by(_w(q, ptr=P, kind=2, nbytes=4736)), P, 64, P, 0, P, gneed, None) == 8
+    assert L.q4nx_gemm_m64(by(w), P, 64, P, 0, None, gneed, None) == 7
+    # repack
+    assert L.q4nx_repack_q4k(None, 4736, 32, 256, P, 5120, None) == 1
+    assert L.q4nx_repack_q4k(P, 4735, 32, 256, P, 5120, None) == 4
+    assert L.q4nx_repack_q4k(P, 4736, 32, 256, P, 5119, None) == 4
+    assert L.q4nx_repack_q4k(P, 4736, 32, 250, P, 5120, None) == 3
+    assert L.q4nx_repack_q4k(P + 1, 4736, 32, 256, P, 5120, None) == 5
+    # argmax
+    assert L.q4nx_argmax(None, 1, 10, P, None) == 1
+    assert L.q4nx_argmax(P, 0, 10, P, None) == 3
+    assert L.q4nx_argmax(P, 1, 0, P, None) == 3
+    assert L.q4nx_argmax(P, 65536, 10, P, None) == 3
+    assert L.q4nx_argmax(P + 2, 1, 10, P, None) == 5
+    assert L.q4nx_check(None, None) == 1
+
+
+def test_weight_tile_rows_is_pointer_arithmetic(q):
+    import torch
+
+    t = torch.zeros(6 * 5120, dtype=torch.uint8)
+    W = q.Weight(t, 1, 96, 512)
+    sub = W.tile_rows(1, 2)
+    assert sub.rows == 64 and sub.cols == 512
+    assert sub.chunks.data_ptr() == t.data_ptr() + 2 * 5120 and sub.chunks.numel() == 4 * 5120
