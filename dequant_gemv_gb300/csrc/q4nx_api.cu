@@ -197,11 +197,10 @@ int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, i
   if (M < 1 || M > 64) return Q4NX_E_M;
   if (out_dtype != Q4NX_OUT_BF16 && out_dtype != Q4NX_OUT_F32) return Q4NX_E_DTYPE;
   if (!aligned16(X_dev) || !aligned16(Y_dev)) return Q4NX_E_ALIGN;
-  if (w->kind == Q4NX_Q4_K) return Q4NX_E_UNSUPPORTED;
+  if (!gemm_supports(w->kind)) return Q4NX_E_UNSUPPORTED;
   if (workspace_dev == nullptr || workspace_bytes < gemm_workspace_bytes(w->rows / 32, w->cols / 256, M))
     return Q4NX_E_WORKSPACE;
   if (!aligned16(workspace_dev)) return Q4NX_E_ALIGN;
-  if (!gemm_available()) return Q4NX_E_UNSUPPORTED;
   return from_cuda(launch_gemm(w->kind, w->chunks_dev, w->rows / 32, w->cols / 256, X_dev, M, Y_dev,
                                out_dtype == Q4NX_OUT_F32, workspace_dev, static_cast<cudaStream_t>(stream)));
 }

@@ -45,6 +45,7 @@ struct GemvItemDev {
   const uint8_t* x;        // bf16 [K]
   void* y;                 // [N]
   int64_t cbase;           // first chunk of this item in the batch index space
+  int64_t nchunks;         // TR * TC
   int32_t TC;
   int32_t trbase;          // first tile row of this item in the batch's counter array
 };
@@ -93,11 +94,10 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
 
 // Finish the segment (item it, tile row tr) of worker wk, whose range starts
 // at lo: `val` is the lane's sum for row `row` of the tile row.
-__device__ __noinline__ void flush_segment(const GemvArgs& a, int64_t wk, int64_t lo, int it, int64_t tr, int row,
-                                           float val, int lane) {
+__device__ __noinline__ void flush_segment(const GemvArgs& a, int64_t wk, int64_t lo, int64_t hi, int it, int64_t tr,
+                                           int row, float val, int lane) {
   const GemvItemDev& item = a.items[it];
   const int64_t row_lo = item.cbase + tr * item.TC, row_hi = row_lo + item.TC;
-  const int64_t hi = (a.T * (wk + 1)) / a.workers;
   const int64_t n = tr * 32 + row;
   if (lo <= row_lo && row_hi <= hi) {               // the whole tile row is ours
     store_y(a, item.y, n, val);
@@ -256,9 +256,13 @@ __device__ __forceinline__ float finish_rows(float (&yacc)[8], int lane, int& ro
 
 // --------------------------------------------------------------- kernel ----
 
-// Cursor over the batch index space: item of chunk c (c only grows).
-struct ItemCursor {
+// Position of a chunk in the batch: item, index inside the item, tile row and
+// column.  Workers walk their ranges in order, so positions advance by one
+// without divisions.
+struct Pos {
   int it;
+  int32_t tr, tc;
+  int64_t local;
   __device__ __forceinline__ void seek(const GemvArgs& a, int64_t c) {
     int lo = 0, hi = a.nitems - 1;                  // last item with cbase <= c
     while (lo < hi) {
@@ -266,22 +270,24 @@ struct ItemCursor {
       if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
     }
     it = lo;
+    local = c - a.items[it].cbase;
+    tr = static_cast<int32_t>(local / a.items[it].TC);
+    tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * a.items[it].TC);
   }
-  __device__ __forceinline__ void advance(const GemvArgs& a, int64_t c) {
-    while (it + 1 < a.nitems && a.items[it + 1].cbase <= c) ++it;
+  __device__ __forceinline__ void next(const GemvArgs& a) {
+    ++local;
+    if (++tc == a.items[it].TC) { tc = 0; ++tr; }
+    if (local == a.items[it].nchunks && it + 1 < a.nitems) { ++it; local = 0; tr = 0; tc = 0; }
   }
 };
 
 template <int KIND>
-__device__ __forceinline__ void issue_stage(const GemvArgs& a, const ItemCursor& cur, int64_t c, uint8_t* dst,
-                                            uint64_t* bar) {
+__device__ __forceinline__ void issue_stage(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  const GemvItemDev& item = a.items[cur.it];
-  const int64_t local = c - item.cbase;
-  const int64_t tc = local % item.TC;
+  const GemvItemDev& item = a.items[p.it];
   mbar_arrive_expect_tx(bar, CB + kXSliceBytes);
-  bulk_g2s(dst, item.chunks + local * CB, CB, bar);
-  bulk_g2s(dst + CB, item.x + tc * kXSliceBytes, kXSliceBytes, bar);
+  bulk_g2s(dst, item.chunks + p.local * CB, CB, bar);
+  bulk_g2s(dst + CB, item.x + static_cast<int64_t>(p.tc) * kXSliceBytes, kXSliceBytes, bar);
 }
 
 template <int KIND>
@@ -296,31 +302,29 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   const int stages = a.stages;
   uint8_t* ring = smem + static_cast<uint64_t>(warp) * stages * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<uint64_t>(nwarps) * stages * SB) + warp * stages;
+  const int n = static_cast<int>(hi - lo);                     // chunks of this worker
 
-  ItemCursor cur, pre;                      // item of the chunk being processed / being fetched
+  Pos cur, pre;                             // chunk being processed / next chunk to fetch
   cur.seek(a, lo);
   pre = cur;
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
-  }
-  __syncwarp();
-  if (lane == 0) {
-    for (int s = 0; s < stages && lo + s < hi; ++s) {
-      pre.advance(a, lo + s);
-      issue_stage<KIND>(a, pre, lo + s, ring + s * SB, &bars[s]);
+    for (int s = 0; s < stages && s < n; ++s) {
+      issue_stage<KIND>(a, pre, ring + s * SB, &bars[s]);
+      pre.next(a);
     }
   }
+  __syncwarp();
 
   float yacc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
-  int seg_it = cur.it;
-  int64_t seg_tr = (lo - a.items[cur.it].cbase) / a.items[cur.it].TC;
+  int seg_it = cur.it, seg_tr = cur.tr;
   uint32_t phase = 0;                       // bit s: parity awaited next on stage s
+  int s = 0;
 
-  for (int64_t c = lo; c < hi; ++c) {
-    const int s = static_cast<int>((c - lo) % stages);
+  for (int j = 0; j < n; ++j) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (phase >> s) & 1u));
     if (!ok) {
       // A wait gave up: record it, let this worker's copies in flight land, stop.
@@ -329,29 +333,29 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
       return;
     }
     phase ^= 1u << s;
-    cur.advance(a, c);
-    const int64_t tr = (c - a.items[cur.it].cbase) / a.items[cur.it].TC;
-    if (cur.it != seg_it || tr != seg_tr) {        // the previous segment is complete
+    if (cur.it != seg_it || cur.tr != seg_tr) {    // the previous segment is complete
       int row;
       const float v = finish_rows<KIND>(yacc, lane, row);
-      flush_segment(a, wk, lo, seg_it, seg_tr, row, v, lane);
+      flush_segment(a, wk, lo, hi, seg_it, seg_tr, row, v, lane);
 #pragma unroll
       for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
       seg_it = cur.it;
-      seg_tr = tr;
+      seg_tr = cur.tr;
     }
     const uint32_t st = smem_u32(ring + s * SB);
     if constexpr (Q4) q4_chunk<KIND>(st, lane, yacc);
     else q8_chunk<KIND>(st, lane, yacc);
     __syncwarp();
-    if (lane == 0 && c + stages < hi) {
-      pre.advance(a, c + stages);
-      issue_stage<KIND>(a, pre, c + stages, ring + s * SB, &bars[s]);
+    if (lane == 0 && j + stages < n) {
+      issue_stage<KIND>(a, pre, ring + s * SB, &bars[s]);
+      pre.next(a);
     }
+    cur.next(a);
+    if (++s == stages) s = 0;
   }
   int row;
   const float v = finish_rows<KIND>(yacc, lane, row);
-  flush_segment(a, wk, lo, seg_it, seg_tr, row, v, lane);
+  flush_segment(a, wk, lo, hi, seg_it, seg_tr, row, v, lane);
 }
 
 // ----------------------------------------------------------------- host ----
@@ -408,6 +412,7 @@ cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f3
     a.items[i].x = static_cast<const uint8_t*>(items[i].x);
     a.items[i].y = items[i].y;
     a.items[i].cbase = T;
+    a.items[i].nchunks = items[i].TR * items[i].TC;
     a.items[i].TC = static_cast<int32_t>(items[i].TC);
     a.items[i].trbase = static_cast<int32_t>(TRsum);
     T += items[i].TR * items[i].TC;

@@ -48,7 +48,7 @@ cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out,
 cudaError_t launch_argmax(const float* logits, int M, int64_t V, int32_t* idx, cudaStream_t s);
 
 // ---- GEMM (M <= 64, tcgen05) ----
-bool gemm_available();
+bool gemm_supports(int kind);
 uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M);
 cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, const void* X, int M, void* Y,
                         int out_f32, void* workspace, cudaStream_t s);

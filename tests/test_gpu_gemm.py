@@ -1,0 +1,94 @@
+"""Parity of the tensor-core decode + GEMM (q4nx_gemm_m64) with the oracle.
+
+Bar: every output within 1e-3 * sum_k |w_k x_k| of the binary64 oracle (plus
+2^-8 |y| for bf16 outputs), per-row cosine >= 0.99999.  The kernel multiplies
+bf16-decoded weights with fp32 accumulation on tcgen05 tensor cores.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from test_gpu_parity import DEV, assert_within, out_values, to_dev_bf16, to_dev_bytes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build()
+    import dequant_gemv_gb300
+
+    return dequant_gemv_gb300
+
+
+def run(q, kind, N, K, M, out="f32", rows=None, seed=0, wid=4):
+    f, w = synth.make(kind, N, K, synth.rng(wid, 0, 50 + seed))
+    X = synth.activations(synth.rng(wid, 0, 60 + seed), M, K)
+    W = q.Weight(to_dev_bytes(w), kind, N, K)
+    Y = out_values(q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype=out))
+    assert Y.shape == (M, N)
+    Y64, A = oracle.matmul(w, kind, N, K, X, rows=rows)
+    assert_within(Y if rows is None else Y[:, rows], Y64, A, out == "bf16", f"gemm {N}x{K} M={M}")
+    return Y
+
+
+@pytest.mark.parametrize("N,K", [(128, 512), (96, 768), (256, 1024), (1024, 1024), (160, 2816), (4224, 512)])
+@pytest.mark.parametrize("M", [64, 1, 17])
+def test_gemm_q4_1_small(q, N, K, M):
+    run(q, synth.Q4_1, N, K, M)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_gemm_q4_1_output_dtypes(q, out):
+    run(q, synth.Q4_1, 512, 1536, 64, out=out)
+
+
+@pytest.mark.parametrize("N,K", [(12288, 4096), (4096, 12288)])
+def test_gemm_prefill_block_8b_width(q, N, K):
+    """The 64-token prefill block at 8B width (gate/up 12288x4096, down 4096x12288)."""
+    rows = np.unique(np.concatenate([np.arange(0, 160), np.arange(N - 160, N),
+                                     np.random.default_rng(2).integers(0, N, 600)]))
+    run(q, synth.Q4_1, N, K, 64, out="bf16", rows=rows)
+
+
+def test_gemm_repeat_runs_are_byte_identical(q):
+    f, w = synth.make(synth.Q4_1, 4096, 12288, synth.rng(4, 0, 70))
+    X = to_dev_bf16(synth.activations(synth.rng(4, 0, 71), 64, 12288))
+    W = q.Weight(to_dev_bytes(w), synth.Q4_1, 4096, 12288)
+    a = q.q4nx_gemm_m64(W, X, out_dtype="f32").clone()
+    b = q.q4nx_gemm_m64(W, X, out_dtype="f32").clone()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    q.q4nx_check(device=DEV)
+
+
+def test_gemm_tokens_beyond_m_untouched(q):
+    """Rows m >= M of the output are neither read nor written."""
+    N, K, M = 256, 512, 5
+    f, w = synth.make(synth.Q4_1, N, K, synth.rng(4, 0, 80))
+    X = synth.activations(synth.rng(4, 0, 81), M, K)
+    W = q.Weight(to_dev_bytes(w), synth.Q4_1, N, K)
+    big = torch.full((8, N), 7.0, dtype=torch.float32, device=DEV)
+    q.q4nx_gemm_m64(W, to_dev_bf16(X), out=big[:M], out_dtype="f32")
+    assert (big[M:] == 7.0).all()
+    Y64, A = oracle.matmul(w, synth.Q4_1, N, K, X)
+    assert_within(out_values(big[:M]), Y64, A, False, "M=5")
+
+
+def test_gemm_matches_gemv_per_token(q):
+    """Each token row of the GEMM agrees with a GEMV of that token (both within
+    tolerance of the oracle; checked against each other at twice the bar)."""
+    N, K, M = 1024, 2048, 8
+    f, w = synth.make(synth.Q4_1, N, K, synth.rng(4, 0, 90))
+    X = synth.activations(synth.rng(4, 0, 91), M, K)
+    W = q.Weight(to_dev_bytes(w), synth.Q4_1, N, K)
+    Xd = to_dev_bf16(X)
+    Y = out_values(q.q4nx_gemm_m64(W, Xd, out_dtype="f32"))
+    _, A = oracle.matmul(w, synth.Q4_1, N, K, X)
+    for m in range(M):
+        y = out_values(q.q4nx_gemv(W, Xd[m].contiguous(), out_dtype="f32"))
+        assert np.all(np.abs(Y[m] - y) <= 2e-3 * A[m])
