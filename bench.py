@@ -348,6 +348,133 @@ def run_gpu(args, rank: int, world: int):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------- suite --
+
+def run_suite(args):
+    """One JSON line per (workload, kernel): every kernel of the path timed on
+    the workload shapes, rotating through weight copies that together exceed
+    512 MB so that no launch finds its weights in L2."""
+    import torch
+
+    import dequant_gemv_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm, _ = _peaks()
+    tc_peak = 1971.6
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            tc_peak = float(json.load(f).get("bf16_tflops", tc_peak))
+    stream = torch.cuda.Stream(dev)
+
+    def copies_for(nbytes):
+        return max(2, min(1024, (512 << 20) // max(nbytes, 1) + 1))
+
+    def timeit(fns, iters):
+        """Time `iters` launches cycling over the callables in `fns` (one per copy), CUDA graph replay."""
+        with torch.cuda.stream(stream):
+            for f in fns:
+                f()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        per_graph = len(fns) * max(1, 64 // len(fns))
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(per_graph):
+                fns[i % len(fns)]()
+        reps = max(1, iters // per_graph)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * per_graph)      # us per launch
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    def dev_bytes(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    cases = [
+        (1, "q4_1 1024x1024", synth.Q4_1, 1024, 1024),
+        (3, "Q4_K 9728x2560", synth.Q4_K, 9728, 2560),
+        (3, "Q4_K 2560x9728", synth.Q4_K, 2560, 9728),
+        (4, "q4_1 12288x4096", synth.Q4_1, 12288, 4096),
+        (4, "q4_1 4096x12288", synth.Q4_1, 4096, 12288),
+        (5, "Q8 KR 151936x2560", synth.Q8_KR, 151936, 2560),
+        (5, "Q8 BLK 151936x2560", synth.Q8_BLK, 151936, 2560),
+    ]
+    only = set(args.only.split(",")) if args.only else None
+    want = lambda k: only is None or k in only
+    for wid, name, kind, N, K in cases:
+        if args.case and args.case not in name:
+            continue
+        f, w = synth.make(kind, N, K, synth.rng(wid, 0, 0))
+        nb = w.size
+        R = copies_for(nb)
+        base = dev_bytes(w)
+        Ws = [q.Weight(base if r == 0 else base.clone(), kind, N, K) for r in range(R)]
+        x = dev_bf16(synth.workload_activations(wid, 0, 1, K)[0])
+        out_f32 = kind in (synth.Q8_KR, synth.Q8_BLK)
+        y = torch.empty(N, dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(max(int(q.lib.q4nx_gemv_workspace(ctypes.byref(Ws[0].c()))), 1 << 16),
+                             dtype=torch.uint8, device=dev)
+        od = "f32" if out_f32 else "bf16"
+        if want("gemv"):
+            us = timeit([lambda W=W: q.q4nx_gemv(W, x, out=y, out_dtype=od, ws=ws) for W in Ws], 400)
+            alg = nb + 2 * K + (4 if out_f32 else 2) * N
+            emit({"suite": "gemv", "workload": name, "M": 1, "us": us, "weight_gbs": nb / us / 1e3,
+                  "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm},
+                  "frac_of_nominal_8tbs": nb / us / 1e3 / 8000.0, "copies": R})
+        if wid in (1, 5) and want("decode"):
+            outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(min(R, 2))]
+            us = timeit([lambda W=W, o=outs[i % len(outs)]: q.q4nx_decode(W, out=o) for i, W in enumerate(Ws)], 64)
+            alg = nb + 2 * N * K
+            emit({"suite": "decode", "workload": name, "us": us, "weight_gbs": nb / us / 1e3,
+                  "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
+            del outs
+        if kind == synth.Q4_K and want("repack"):
+            rep = torch.empty((N // 32) * (K // 256) * 5120, dtype=torch.uint8, device=dev)
+            us = timeit([lambda W=W: q.q4nx_repack_q4k(W.chunks, N, K, out=rep) for W in Ws], 400)
+            alg = nb + rep.numel()
+            emit({"suite": "repack", "workload": name, "us": us,
+                  "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
+        if kind == synth.Q4_1 and wid == 4 and want("gemm_m64"):
+            M = 64
+            X = dev_bf16(synth.workload_activations(wid, 0, M, K))
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            with torch.cuda.stream(stream):
+                gws = torch.zeros(int(q.lib.q4nx_gemm_workspace(ctypes.byref(Ws[0].c()), M)), dtype=torch.uint8,
+                                  device=dev)
+            us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, ws=gws) for W in Ws], 400)
+            flops = 2.0 * M * N * K
+            alg = nb + 2 * M * K + 2 * M * N
+            t_roof = max(alg / (hbm * 1e3), flops / (tc_peak * 1e6))
+            emit({"suite": "gemm_m64", "workload": name, "M": M, "us": us, "tflops": flops / us / 1e6,
+                  "weight_gbs": nb / us / 1e3,
+                  "roofline": {"bound": "hbm" if alg / (hbm * 1e3) >= flops / (tc_peak * 1e6) else "tensor",
+                               "roofline_us": t_roof, "frac": t_roof / us, "hbm_peak": hbm, "tensor_peak": tc_peak}})
+        if wid == 5 and want("argmax"):
+            for M in (1, 64):
+                L = torch.randn((M, N), generator=torch.Generator(device="cpu").manual_seed(M), dtype=torch.float32).to(dev)
+                idx = torch.empty(M, dtype=torch.int32, device=dev)
+                Ls = [L] + [L.clone() for _ in range(max(1, min(1024, (512 << 20) // L.numel() // 4)))]
+                us = timeit([lambda Lm=Lm: q.q4nx_argmax(Lm, out=idx) for Lm in Ls], 400)
+                emit({"suite": "argmax", "workload": f"logits {M}x{N}", "us": us,
+                      "roofline": {"bound": "hbm", "achieved": 4 * M * N / us / 1e3, "peak": hbm,
+                                   "frac": 4 * M * N / us / 1e3 / hbm}})
+        del Ws, base
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -357,6 +484,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
+    ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
+    ap.add_argument("--only", default="", help="suite: comma list of gemv,decode,repack,gemm_m64,argmax")
+    ap.add_argument("--case", default="", help="suite: substring of the workload name")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -364,6 +494,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.suite:
+        run_suite(args)
         return
     if world > 1:
         import torch.distributed as dist

@@ -5,25 +5,27 @@
 //   section of the 1bit engine "NPU engine" page: code*scale + zero).
 //
 // Tile: 128 weight rows (4 tile rows of the chunk grid) x 64 tokens; k-steps
-// of 256 columns (one chunk column).  The weight rows are the MMA's M side,
-// the tokens its N side, so one tcgen05.mma (M=128, N=64, K=16, bf16 x bf16
-// -> fp32 in TMEM) covers a whole token block.
-// Warp roles in a CTA of 14 warps:
-//   warp 0      TMA producer: per k-step the 4 chunks' code regions (3-D tensor
-//               copy with 128-byte swizzle), their scale/zero regions (1-D bulk
-//               copies) and the X tile (4 boxes of 64 k x 64 tokens, 128-byte
-//               swizzle), into one of 2 raw stages;
-//   warp 1      TMEM allocator and MMA issuer (one thread);
-//   warps 2-9   dequant: warp d decodes tile row d%4, k-half d/4 of the step,
-//               one thread per weight row, into bf16 A tiles in the canonical
-//               K-major 128-byte-swizzled layout (3 A stages of K = 128);
-//   warps 10-13 epilogue: TMEM -> registers -> Y (or a split-K partial).
+// of 256 columns (one chunk column).  The weight rows are the MMA's M side and
+// the tokens its N side, so one tcgen05.mma (M=128, N=64, K=16, bf16 x bf16 ->
+// fp32 in TMEM) covers the whole token block.
+//
+// Warp roles (23 warps):
+//   warp 0       weight producer: per k-step the 4 chunks' code regions (3-D
+//                tensor copy, 128-byte swizzle) and scale/zero regions (1-D
+//                bulk copies) into one of 4 weight stages;
+//   warp 1       X producer: the 64 x 256 bf16 X slice of the k-step (4 boxes of
+//                64 x 64, 128-byte swizzle) into one of 2 X stages;
+//   warp 2       TMEM allocator and MMA issuer (one thread);
+//   warps 3-18   dequant: warp d decodes tile row d%4, columns 64(d/4)..+63 of
+//                the step, one thread per weight row, into A stage d/4 (bf16,
+//                canonical K-major 128-byte-swizzled layout, 128 x 64);
+//   warps 19-22  epilogue: TMEM -> registers -> Y, or a split-K partial.
 // Two accumulators in TMEM (2 x 64 columns) let the epilogue of one tile
-// overlap the main loop of the next.  Work is spread stream-K style: every
-// CTA owns a contiguous range of (tile, k-step) units; a tile split between
-// CTAs is finished by the last CTA to arrive, which adds the fp32 partials in
-// CTA order.  Every wait is bounded; if one gives up, the CTA sets a shared
-// abort flag, records the error in the workspace and winds down.
+// overlap the main loop of the next.  Work is spread stream-K style: every CTA
+// owns a contiguous range of (tile, k-step) units; a tile split between CTAs
+// is finished by the last CTA to arrive, which adds the fp32 partials in CTA
+// order (deterministic).  Every wait is bounded; if one gives up, the CTA sets
+// a shared abort flag, records the error in the workspace and winds down.
 #include <cuda.h>
 
 #include "q4nx_device.cuh"
@@ -33,20 +35,22 @@ namespace q4nx {
 namespace gemm {
 
 constexpr int kTileM = 128, kTileN = 64, kStepK = 256;
-constexpr int kRawStages = 2, kAStages = 3, kAccs = 2;
+constexpr int kWStages = 4, kXStages = 2, kAStages = 4, kAccs = 2;
 constexpr int kCodes = 4096, kScales = 1024;
-constexpr int kXBox = 64 * 128;                      // 64 tokens x 64 k of bf16
-constexpr int kRawCodes = 0;                         // 4 x 4096, 1024-aligned
-constexpr int kRawX = 4 * kCodes;                    // 4 x 8192
-constexpr int kRawScales = kRawX + 4 * kXBox;        // 4 x 1024
-constexpr int kRawBytes = kRawScales + 4 * kScales;  // 53248
-constexpr int kABlock = 128 * 128;                   // 128 rows x 64 k of bf16
-constexpr int kABytes = 2 * kABlock;                 // K = 128 per A stage
-constexpr int kAOff = kRawStages * kRawBytes;
+constexpr int kWBytes = 4 * kCodes + 4 * kScales;     // 20 KB: codes (1024-aligned) then scales
+constexpr int kXBox = 64 * 128;                        // 64 tokens x 64 k of bf16
+constexpr int kXBytes = 4 * kXBox;                     // 32 KB
+constexpr int kABytes = 128 * 128;                     // 128 rows x 64 k of bf16
+constexpr int kWOff = 0;
+constexpr int kXOff = kWOff + kWStages * kWBytes;
+constexpr int kAOff = kXOff + kXStages * kXBytes;
 constexpr int kBarOff = kAOff + kAStages * kABytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;     // barriers, flags, alignment slack
-constexpr int kThreads = 14 * 32;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpDequant0 = 2, kWarpEpi0 = 10;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;       // barriers and flags, alignment slack
+constexpr int kDequantWarps = 16;
+constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpDequant0 = 3, kWarpEpi0 = kWarpDequant0 + kDequantWarps;
+constexpr int kWarps = kWarpEpi0 + 4;
+constexpr int kThreads = kWarps * 32;
+static_assert(kWStages * kWBytes % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions must stay 1024-aligned");
 
 // tcgen05 instruction descriptor: D fp32, A bf16, B bf16, both K-major, N = 64, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kTileN >> 3) << 17) | ((kTileM >> 4) << 24);
@@ -79,9 +83,7 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -123,12 +125,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 struct Shared {
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t x_full[kXStages], x_empty[kXStages];
   uint64_t a_full[kAStages], a_empty[kAStages];
   uint64_t acc_full[kAccs], acc_empty[kAccs];
   uint64_t drain;
@@ -136,6 +144,7 @@ struct Shared {
   volatile uint32_t abort_flag;
   uint32_t last_flag;
 };
+static_assert(sizeof(Shared) <= 256, "barrier block");
 
 // Bounded wait that also gives up at once when another warp has aborted.
 __device__ __forceinline__ bool wait_bar(Shared* sh, uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -152,13 +161,55 @@ __device__ __forceinline__ bool wait_bar(Shared* sh, uint64_t* bar, uint32_t par
   }
 }
 
-// Y[m][n] for m < M of one weight row n (fully unrolled: acc stays in registers)
-__device__ __forceinline__ void store_rows(const Args& a, int64_t n, const float (&acc)[64]) {
+// One 32-token slice of an output row: Y[m][n] for m in [m0, m0 + 32), m < M.
+__device__ __forceinline__ void store_slice(const Args& a, int64_t n, int m0, const float (&v)[32]) {
 #pragma unroll
-  for (int m = 0; m < kTileN; ++m) {
+  for (int i = 0; i < 32; ++i) {
+    const int m = m0 + i;
     if (m < a.M) {
-      if (a.out_f32) static_cast<float*>(a.Y)[m * a.N + n] = acc[m];
-      else static_cast<uint16_t*>(a.Y)[m * a.N + n] = f32_to_bf16_bits(acc[m]);
+      if (a.out_f32) static_cast<float*>(a.Y)[m * a.N + n] = v[i];
+      else static_cast<uint16_t*>(a.Y)[m * a.N + n] = f32_to_bf16_bits(v[i]);
+    }
+  }
+}
+
+// Decode columns [64 qq, 64 qq + 64) of weight row r of one tile row (its
+// 128-byte-swizzled code region and its scale/zero region) into row rowA of
+// an A stage (128 x 64 bf16, K-major, 128-byte swizzle).
+__device__ __forceinline__ void dequant_quarter(uint32_t codes, uint32_t scales, int r, int qq, uint32_t abase,
+                                                int rowA) {
+  // scales and zeros of groups 2qq, 2qq+1: one bf16 pair each
+  const uint32_t sw = lds_u32(scales + r * 16 + qq * 4);
+  const uint32_t zw = lds_u32(scales + 512 + r * 16 + qq * 4);
+#pragma unroll
+  for (int gg = 0; gg < 2; ++gg) {
+    const int g = 2 * qq + gg;
+    const float s = __uint_as_float(gg ? (sw & 0xFFFF0000u) : (sw << 16));
+    const float z = __uint_as_float(gg ? (zw & 0xFFFF0000u) : (zw << 16));
+    // w = (1 + c 2^-8)(256 s) + (z - 256 s) for even k, (1 + c 2^-4)(16 s) + (z - 16 s) for odd k
+    const float2 s2 = make_float2(s * 256.f, s * 16.f);
+    const float2 z2 = make_float2(z - s2.x, z - s2.y);
+    const uint4 cw = lds128(codes + r * 128 + ((g ^ (r & 7)) << 4));
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t ONE = 0x3F800000u;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t w = words[t];
+      const uint32_t a15 = w << 15, a7 = w << 7, b1 = w >> 1, b9 = w >> 9;
+      const float2 v0 = make_float2(__uint_as_float(lop3_and_or(a15, 0x00078000u, ONE)),
+                                    __uint_as_float(lop3_and_or(a15, 0x00780000u, ONE)));
+      const float2 v1 = make_float2(__uint_as_float(lop3_and_or(a7, 0x00078000u, ONE)),
+                                    __uint_as_float(lop3_and_or(a7, 0x00780000u, ONE)));
+      const float2 v2 = make_float2(__uint_as_float(lop3_and_or(b1, 0x00078000u, ONE)),
+                                    __uint_as_float(lop3_and_or(b1, 0x00780000u, ONE)));
+      const float2 v3 = make_float2(__uint_as_float(lop3_and_or(b9, 0x00078000u, ONE)),
+                                    __uint_as_float(lop3_and_or(b9, 0x00780000u, ONE)));
+      const float2 w0 = ffma2(v0, s2, z2), w1 = ffma2(v1, s2, z2);
+      const float2 w2 = ffma2(v2, s2, z2), w3 = ffma2(v3, s2, z2);
+      // k within the stage = 32 gg + 8 t: 16-byte unit (4 gg + t) of the 128-byte row
+      const int unit = 4 * gg + t;
+      sts128(abase + rowA * 128 + ((unit ^ (rowA & 7)) << 4), pack_bf16x2(w0.x, w0.y), pack_bf16x2(w1.x, w1.y),
+             pack_bf16x2(w2.x, w2.y), pack_bf16x2(w3.x, w3.y));
     }
   }
 }
@@ -177,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = static_cast<int>(last_tile - first_tile + 1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) { mbar_init(&sh->raw_full[s], 1); mbar_init(&sh->raw_empty[s], 9); }
+    for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantWarps); }
+    for (int s = 0; s < kXStages; ++s) { mbar_init(&sh->x_full[s], 1); mbar_init(&sh->x_empty[s], 1); }
     for (int s = 0; s < kAStages; ++s) { mbar_init(&sh->a_full[s], 4); mbar_init(&sh->a_empty[s], 1); }
     for (int s = 0; s < kAccs; ++s) { mbar_init(&sh->acc_full[s], 1); mbar_init(&sh->acc_empty[s], 4); }
     mbar_init(&sh->drain, 1);
@@ -195,204 +247,174 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
 
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
+  if (warp == kWarpW) {
+    // ----------------------------------------------------------- weights
     if (lane == 0) {
       int64_t tile = lo / KS, ks = lo - tile * KS;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kRawStages;
-        const uint32_t ph = (j / kRawStages) & 1;
-        if (!wait_bar(sh, &sh->raw_empty[s], ph ^ 1u, a.err)) break;
-        uint8_t* raw = smem + s * kRawBytes;
+      int j = 0;
+      for (; j < n; ++j) {
+        const int s = j % kWStages;
+        if (!wait_bar(sh, &sh->w_empty[s], ((j / kWStages) & 1) ^ 1u, a.err)) break;
+        uint8_t* st = smem + kWOff + s * kWBytes;
         const int64_t left = a.TR - tile * 4;
         const int rows = left < 4 ? static_cast<int>(left) : 4;
-        mbar_arrive_expect_tx(&sh->raw_full[s], rows * (kCodes + kScales) + 4 * kXBox);
+        mbar_arrive_expect_tx(&sh->w_full[s], rows * (kCodes + kScales));
         for (int i = 0; i < rows; ++i) {
           const int64_t chunk = (tile * 4 + i) * a.TC + ks;
-          tma_3d(raw + kRawCodes + i * kCodes, &wmap, 0, 0, static_cast<int>(chunk), &sh->raw_full[s]);
-          bulk_g2s(raw + kRawScales + i * kScales, a.chunks + chunk * kQ41Bytes + kQ41Scale, kScales,
-                   &sh->raw_full[s]);
+          tma_3d(st + i * kCodes, &wmap, 0, 0, static_cast<int>(chunk), &sh->w_full[s]);
+          bulk_g2s(st + 4 * kCodes + i * kScales, a.chunks + chunk * kQ41Bytes + kQ41Scale, kScales, &sh->w_full[s]);
         }
-        for (int b = 0; b < 4; ++b)
-          tma_2d(raw + kRawX + b * kXBox, &xmap, static_cast<int>(ks * kStepK + b * 64), 0, &sh->raw_full[s]);
         if (++ks == KS) { ks = 0; ++tile; }
       }
-      // let the last copies land before the CTA can finish
-      for (int j = (n > kRawStages ? n - kRawStages : 0); j < n; ++j)
-        mbar_wait_bounded(&sh->raw_full[j % kRawStages], (j / kRawStages) & 1, 100000000ull);
+      for (int t = (j > kWStages ? j - kWStages : 0); t < j; ++t)      // copies still in flight land first
+        mbar_wait_bounded(&sh->w_full[t % kWStages], (t / kWStages) & 1, 100000000ull);
+    }
+  } else if (warp == kWarpX) {
+    // ----------------------------------------------------------- X
+    if (lane == 0) {
+      int64_t ks = lo % KS;
+      int j = 0;
+      for (; j < n; ++j) {
+        const int s = j % kXStages;
+        if (!wait_bar(sh, &sh->x_empty[s], ((j / kXStages) & 1) ^ 1u, a.err)) break;
+        uint8_t* st = smem + kXOff + s * kXBytes;
+        mbar_arrive_expect_tx(&sh->x_full[s], kXBytes);
+        for (int b = 0; b < 4; ++b)
+          tma_2d(st + b * kXBox, &xmap, static_cast<int>(ks * kStepK + b * 64), 0, &sh->x_full[s]);
+        if (++ks == KS) ks = 0;
+      }
+      for (int t = (j > kXStages ? j - kXStages : 0); t < j; ++t)
+        mbar_wait_bounded(&sh->x_full[t % kXStages], (t / kXStages) & 1, 100000000ull);
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int64_t tile = lo / KS, ks = lo - tile * KS;
+      int64_t ks = lo % KS;
       int tcount = 0;
       bool first_in_tile = true;
-      bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
+      for (int j = 0; j < n; ++j) {
         const int b = tcount % kAccs;
         if (first_in_tile) {
-          ok = wait_bar(sh, &sh->acc_empty[b], ((tcount / kAccs) & 1) ^ 1u, a.err);
-          if (!ok) break;
+          if (!wait_bar(sh, &sh->acc_empty[b], ((tcount / kAccs) & 1) ^ 1u, a.err)) break;
           tc_fence_after();
         }
-        const int rs = j % kRawStages;
-        ok = wait_bar(sh, &sh->raw_full[rs], (j / kRawStages) & 1, a.err);
-        if (!ok) break;
-        const uint32_t xbase = smem_u32(smem + rs * kRawBytes + kRawX);
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int u = 2 * j + h;
-          const int as = u % kAStages;
-          ok = wait_bar(sh, &sh->a_full[as], (u / kAStages) & 1, a.err);
-          if (!ok) break;
+        const int xs = j % kXStages;
+        if (!wait_bar(sh, &sh->x_full[xs], (j / kXStages) & 1, a.err)) break;
+        const uint32_t xbase = smem_u32(smem + kXOff + xs * kXBytes);
+        bool ok = true;
+        for (int q = 0; q < kAStages; ++q) {
+          if (!wait_bar(sh, &sh->a_full[q], j & 1, a.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t abase = smem_u32(smem + kAOff + as * kABytes);
+          const uint32_t abase = smem_u32(smem + kAOff + q * kABytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sw128_desc(abase + (kk >> 2) * kABlock + (kk & 3) * 32);
-            const uint64_t bd = sw128_desc(xbase + (2 * h + (kk >> 2)) * kXBox + (kk & 3) * 32);
-            mma_bf16(tmem + b * kTileN, ad, bd, (first_in_tile && h == 0 && kk == 0) ? 0u : 1u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_desc(abase + kk * 32);
+            const uint64_t bd = sw128_desc(xbase + q * kXBox + kk * 32);
+            mma_bf16(tmem + b * kTileN, ad, bd, (first_in_tile && q == 0 && kk == 0) ? 0u : 1u);
           }
-          mma_commit(&sh->a_empty[as]);
+          mma_commit(&sh->a_empty[q]);
         }
         if (!ok) break;
-        mma_commit(&sh->raw_empty[rs]);
+        mma_commit(&sh->x_empty[xs]);
         first_in_tile = false;
-        if (++ks == KS || j == n - 1) {             // this CTA's part of the tile is complete
+        if (++ks == KS || j == n - 1) {             // this CTA's share of the tile is complete
           mma_commit(&sh->acc_full[b]);
           ++tcount;
           first_in_tile = true;
-          if (ks == KS) { ks = 0; ++tile; }
+          if (ks == KS) ks = 0;
         }
       }
-      // drain: wait until every MMA issued so far has completed
-      mma_commit(&sh->drain);
+      mma_commit(&sh->drain);                       // every MMA issued so far has completed
       mbar_wait_bounded(&sh->drain, 0, 100000000ull);
     }
   } else if (warp < kWarpEpi0) {
-    // ------------------------------------------------------------ dequant
+    // ----------------------------------------------------------- dequant
     const int d = warp - kWarpDequant0;
-    const int i = d & 3, h = d >> 2;
-    const int r = lane;
-    const int rowA = 32 * i + r;
-    int64_t tile = lo / KS;
+    const int i = d & 3, qq = d >> 2;
+    const int rowA = 32 * i + lane;
+    const uint32_t abase = smem_u32(smem + kAOff + qq * kABytes);
+    int64_t tile = lo / KS, ks = lo - tile * KS;
     for (int j = 0; j < n; ++j) {
-      const int rs = j % kRawStages;
-      if (!wait_bar(sh, &sh->raw_full[rs], (j / kRawStages) & 1, a.err)) break;
-      const int u = 2 * j + h;
-      const int as = u % kAStages;
-      if (!wait_bar(sh, &sh->a_empty[as], ((u / kAStages) & 1) ^ 1u, a.err)) break;
-      const uint8_t* raw = smem + rs * kRawBytes;
+      const int s = j % kWStages;
+      if (!wait_bar(sh, &sh->w_full[s], (j / kWStages) & 1, a.err)) break;
+      if (!wait_bar(sh, &sh->a_empty[qq], (j & 1) ^ 1u, a.err)) break;
       if (tile * 4 + i < a.TR) {
-        const uint32_t cbase = smem_u32(raw + kRawCodes + i * kCodes) + r * 128;
-        const uint4 srow = lds128(smem_u32(raw + kRawScales + i * kScales) + r * 16);
-        const uint4 zrow = lds128(smem_u32(raw + kRawScales + i * kScales + 512) + r * 16);
-        const uint32_t sw[4] = {srow.x, srow.y, srow.z, srow.w};
-        const uint32_t zw[4] = {zrow.x, zrow.y, zrow.z, zrow.w};
-        const uint32_t abase = smem_u32(smem + kAOff + as * kABytes);
-#pragma unroll
-        for (int gg = 0; gg < 4; ++gg) {
-          const int g = 4 * h + gg;
-          const float s = __uint_as_float((g & 1) ? (sw[g >> 1] & 0xFFFF0000u) : (sw[g >> 1] << 16));
-          const float z = __uint_as_float((g & 1) ? (zw[g >> 1] & 0xFFFF0000u) : (zw[g >> 1] << 16));
-          // w = (1 + c 2^-8) (256 s) + (z - 256 s) for even k, (1 + c 2^-4) (16 s) + (z - 16 s) for odd k
-          const float2 s2 = make_float2(s * 256.f, s * 16.f);
-          const float2 z2 = make_float2(z - s2.x, z - s2.y);
-          const uint4 cw = lds128(cbase + ((g ^ (r & 7)) << 4));
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-          const uint32_t ONE = 0x3F800000u;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t w = words[t];
-            const uint32_t sh15 = w << 15, sh7 = w << 7, sr1 = w >> 1, sr9 = w >> 9;
-            const float2 v0 = make_float2(__uint_as_float(lop3_and_or(sh15, 0x00078000u, ONE)),
-                                          __uint_as_float(lop3_and_or(sh15, 0x00780000u, ONE)));
-            const float2 v1 = make_float2(__uint_as_float(lop3_and_or(sh7, 0x00078000u, ONE)),
-                                          __uint_as_float(lop3_and_or(sh7, 0x00780000u, ONE)));
-            const float2 v2 = make_float2(__uint_as_float(lop3_and_or(sr1, 0x00078000u, ONE)),
-                                          __uint_as_float(lop3_and_or(sr1, 0x00780000u, ONE)));
-            const float2 v3 = make_float2(__uint_as_float(lop3_and_or(sr9, 0x00078000u, ONE)),
-                                          __uint_as_float(lop3_and_or(sr9, 0x00780000u, ONE)));
-            const float2 w0 = ffma2(v0, s2, z2), w1 = ffma2(v1, s2, z2);
-            const float2 w2 = ffma2(v2, s2, z2), w3 = ffma2(v3, s2, z2);
-            // k (within the 128-wide A stage) = 32 gg + 8 t .. +7: block (32 gg + 8 t) / 64, unit ((32 gg + 8 t) % 64) / 8
-            const int kk = 32 * gg + 8 * t;
-            const int unit = (kk & 63) >> 3;
-            const uint32_t dst = abase + (kk >> 6) * kABlock + rowA * 128 + ((unit ^ (rowA & 7)) << 4);
-            sts128(dst, pack_bf16x2(w0.x, w0.y), pack_bf16x2(w1.x, w1.y), pack_bf16x2(w2.x, w2.y),
-                   pack_bf16x2(w3.x, w3.y));
-          }
-        }
+        const uint32_t st = smem_u32(smem + kWOff + s * kWBytes);
+        dequant_quarter(st + i * kCodes, st + 4 * kCodes + i * kScales, lane, qq, abase, rowA);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sh->a_full[as]);
-        mbar_arrive(&sh->raw_empty[rs]);
+        mbar_arrive(&sh->a_full[qq]);
+        mbar_arrive(&sh->w_empty[s]);
       }
-      if (lo + j + 1 < hi && (lo + j + 1) % KS == 0) ++tile;
+      if (++ks == KS) { ks = 0; ++tile; }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ----------------------------------------------------------- epilogue
     const int e = warp & 3;                         // TMEM lane quarter of this warp
     const int row = 32 * e + lane;                  // row within the 128-row tile
     for (int t = 0; t < ntiles; ++t) {
       const int b = t % kAccs;
       if (!wait_bar(sh, &sh->acc_full[b], (t / kAccs) & 1, a.err)) break;
       tc_fence_after();
-      float acc[64];
-      float (&lo32)[32] = *reinterpret_cast<float(*)[32]>(&acc[0]);
-      float (&hi32)[32] = *reinterpret_cast<float(*)[32]>(&acc[32]);
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + b * kTileN;
-      tmem_ld32(taddr, lo32);
-      tmem_ld32(taddr + 32, hi32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
-
       const int64_t tile = first_tile + t;
       const int64_t u_lo = tile * KS, u_hi = u_lo + KS;
       const int64_t n0 = tile * kTileM;
       const bool valid_row = n0 + row < a.N;
-      if (lo <= u_lo && u_hi <= hi) {              // whole tile computed here
-        if (valid_row) store_rows(a, n0 + row, acc);
-        continue;
-      }
-      // split tile: park the partial, the last CTA to arrive finishes it
-      const int slot = (lo >= u_lo) ? 0 : 1;
-      float* mine = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * (kTileN * kTileM);
+      const bool whole = lo <= u_lo && u_hi <= hi;   // the whole tile was computed here
+      const int slot = (lo >= u_lo) ? 0 : 1;          // split tile: this CTA's partial slot
+      float* mine = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * (kTileN * kTileM) + row;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + b * kTileN;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        tmem_ld32(taddr + 32 * h, v);
+        if (whole) {
+          if (valid_row) store_slice(a, n0 + row, 32 * h, v);
+        } else {
 #pragma unroll
-      for (int m = 0; m < kTileN; ++m)
-        if (m < a.M) mine[m * kTileM + row] = acc[m];
+          for (int m = 0; m < 32; ++m) mine[(32 * h + m) * kTileM] = v[m];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
+      if (whole) continue;
+      // split tile: the last CTA to arrive adds the partials (in CTA order) and stores the tile
       __threadfence();
       named_bar(1, 128);
       const int64_t c_first = ((u_lo + 1) * a.grid - 1) / a.units;
-      const int64_t c_last = ((u_hi - 1 + 1) * a.grid - 1) / a.units;
+      const int64_t c_last = (u_hi * a.grid - 1) / a.units;
       if (threadIdx.x == kWarpEpi0 * 32) {
         const uint32_t old = atomicAdd(&a.counters[tile], 1u);
         sh->last_flag = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
       }
       named_bar(1, 128);
-      if (!sh->last_flag) continue;
+      const bool last = sh->last_flag != 0u;
+      named_bar(1, 128);                            // every thread has read the flag before it is reused
+      if (!last) continue;
       __threadfence();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
 #pragma unroll
-      for (int m = 0; m < kTileN; ++m) acc[m] = 0.f;
-      for (int64_t c = c_first; c <= c_last; ++c) {
-        const int64_t clo = a.units * c / a.grid;
-        float* p = a.partials + (c * 2 + ((clo >= u_lo) ? 0 : 1)) * (kTileN * kTileM);
+        for (int m = 0; m < 32; ++m) v[m] = 0.f;
+        for (int64_t c = c_first; c <= c_last; ++c) {
+          const int64_t clo = a.units * c / a.grid;
+          float* p = a.partials + (c * 2 + ((clo >= u_lo) ? 0 : 1)) * (kTileN * kTileM) + row + 32 * h * kTileM;
 #pragma unroll
-        for (int m = 0; m < kTileN; ++m) {
-          if (m < a.M) {
-            acc[m] += ld_cg_f32(p + m * kTileM + row);
-            p[m * kTileM + row] = 0.f;             // leave the workspace zero-filled
-          }
+          for (int m = 0; m < 32; ++m) v[m] += ld_cg_f32(p + m * kTileM);
+#pragma unroll
+          for (int m = 0; m < 32; ++m) p[m * kTileM] = 0.f;    // leave the workspace zero-filled
         }
+        if (valid_row) store_slice(a, n0 + row, 32 * h, v);
       }
-      if (valid_row) store_rows(a, n0 + row, acc);
-      named_bar(1, 128);
       if (threadIdx.x == kWarpEpi0 * 32) a.counters[tile] = 0u;
     }
   }
 
+  __syncwarp();                                     // whole warps arrive at the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -429,7 +451,7 @@ uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M) {
   (void)TC;
   (void)M;
   const int64_t tiles = (TR + 3) / 4;
-  // partial tiles of at most 1024 CTAs (more SMs than any current part)
+  // error word, arrival counters, partial tiles of at most 1024 CTAs
   return kWsErrBytes + align16(static_cast<uint64_t>(tiles) * 4) +
          static_cast<uint64_t>(1024) * 2 * gemm::kTileN * gemm::kTileM * 4;
 }

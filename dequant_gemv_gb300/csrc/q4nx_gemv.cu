@@ -50,8 +50,11 @@ struct GemvItemDev {
   int32_t trbase;          // first tile row of this item in the batch's counter array
 };
 
-struct GemvArgs {
-  GemvItemDev items[kMaxBatch];
+// Kernel parameters; MAXB batch slots (instantiated for 1, 8 and 256 items so
+// that small launches do not carry a 12 KB parameter block).
+template <int MAXB>
+struct GemvArgsT {
+  GemvItemDev items[MAXB];
   int nitems;
   int workers;
   int stages;
@@ -87,6 +90,7 @@ __device__ __forceinline__ float transpose_reduce8(float v[8], int lane, int m2,
 // worker that holds chunk c: the largest w with floor(T*w/W) <= c
 __device__ __forceinline__ int64_t worker_of(int64_t c, int64_t T, int64_t W) { return ((c + 1) * W - 1) / T; }
 
+template <class GemvArgs>
 __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, float v) {
   if (a.out_f32) static_cast<float*>(y)[n] = v;
   else static_cast<uint16_t*>(y)[n] = f32_to_bf16_bits(v);
@@ -94,6 +98,7 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
 
 // Finish the segment (item it, tile row tr) of worker wk, whose range starts
 // at lo: `val` is the lane's sum for row `row` of the tile row.
+template <class GemvArgs>
 __device__ __noinline__ void flush_segment(const GemvArgs& a, int64_t wk, int64_t lo, int64_t hi, int it, int64_t tr,
                                            int row, float val, int lane) {
   const GemvItemDev& item = a.items[it];
@@ -263,6 +268,7 @@ struct Pos {
   int it;
   int32_t tr, tc;
   int64_t local;
+  template <class GemvArgs>
   __device__ __forceinline__ void seek(const GemvArgs& a, int64_t c) {
     int lo = 0, hi = a.nitems - 1;                  // last item with cbase <= c
     while (lo < hi) {
@@ -274,6 +280,7 @@ struct Pos {
     tr = static_cast<int32_t>(local / a.items[it].TC);
     tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * a.items[it].TC);
   }
+  template <class GemvArgs>
   __device__ __forceinline__ void next(const GemvArgs& a) {
     ++local;
     if (++tc == a.items[it].TC) { tc = 0; ++tr; }
@@ -281,7 +288,7 @@ struct Pos {
   }
 };
 
-template <int KIND>
+template <int KIND, class GemvArgs>
 __device__ __forceinline__ void issue_stage(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
   const GemvItemDev& item = a.items[p.it];
@@ -290,8 +297,8 @@ __device__ __forceinline__ void issue_stage(const GemvArgs& a, const Pos& p, uin
   bulk_g2s(dst + CB, item.x + static_cast<int64_t>(p.tc) * kXSliceBytes, kXSliceBytes, bar);
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ GemvArgs a) {
+template <int KIND, int MAXB>
+__global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = chunk_bytes_of(KIND) + kXSliceBytes;     // stage bytes
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
@@ -394,18 +401,19 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks) {
   return kWsErrBytes + align16(static_cast<uint64_t>(total_tile_rows) * 4) + static_cast<uint64_t>(w) * 2 * 32 * 4;
 }
 
-template <int KIND>
-static cudaError_t launch_gemv_t(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND>), KIND);
+template <int KIND, int MAXB>
+static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
+  const int slot = KIND + (MAXB == 1 ? 0 : MAXB == 8 ? 4 : 8);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB>), slot);
   if (e != cudaSuccess) return e;
-  gemv_kernel<KIND><<<p.grid, p.warps * 32, p.smem, s>>>(a);
+  gemv_kernel<KIND, MAXB><<<p.grid, p.warps * 32, p.smem, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
-                              int max_smem, cudaStream_t s) {
-  if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
-  GemvArgs a;
+template <int MAXB>
+static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
+                                     int max_smem, cudaStream_t s) {
+  GemvArgsT<MAXB> a;
   int64_t T = 0, TRsum = 0;
   for (int i = 0; i < n; ++i) {
     a.items[i].chunks = static_cast<const uint8_t*>(items[i].chunks);
@@ -430,12 +438,20 @@ cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f3
   a.counters = reinterpret_cast<uint32_t*>(ws + kWsErrBytes);
   a.partials = reinterpret_cast<float*>(ws + kWsErrBytes + align16(static_cast<uint64_t>(TRsum) * 4));
   switch (kind) {
-    case kQ4_1: return launch_gemv_t<kQ4_1>(a, p, s);
-    case kQ4_K: return launch_gemv_t<kQ4_K>(a, p, s);
-    case kQ8_KR: return launch_gemv_t<kQ8_KR>(a, p, s);
-    case kQ8_BLK: return launch_gemv_t<kQ8_BLK>(a, p, s);
+    case kQ4_1: return launch_gemv_t<kQ4_1, MAXB>(a, p, s);
+    case kQ4_K: return launch_gemv_t<kQ4_K, MAXB>(a, p, s);
+    case kQ8_KR: return launch_gemv_t<kQ8_KR, MAXB>(a, p, s);
+    case kQ8_BLK: return launch_gemv_t<kQ8_BLK, MAXB>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
+                              int max_smem, cudaStream_t s) {
+  if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
+  if (n == 1) return launch_gemv_sized<1>(kind, items, n, out_f32, workspace, sms, max_smem, s);
+  if (n <= 8) return launch_gemv_sized<8>(kind, items, n, out_f32, workspace, sms, max_smem, s);
+  return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, sms, max_smem, s);
 }
 
 }  // namespace q4nx
