@@ -38,6 +38,8 @@
 namespace q4nx {
 
 constexpr int kXSliceBytes = 512;            // bf16 x of one tile column
+constexpr int kScratchBytes = 512;           // per warp: x byte planes of one chunk
+constexpr int kSlotBytes = 2 * 32 * 4;       // per warp: sums of its first and last tile row
 constexpr int kMaxBatch = kMaxGemvItems;
 
 struct GemvItemDev {
@@ -56,13 +58,13 @@ template <int MAXB>
 struct GemvArgsT {
   GemvItemDev items[MAXB];
   int nitems;
-  int workers;
+  int grid;                // CTAs; CTA b owns chunks [T b / grid, T (b+1) / grid)
   int stages;
   int out_f32;
   int64_t T;               // chunks in the batch
   uint32_t* err;
   uint32_t* counters;      // [sum TR]
-  float* partials;         // [workers][2][32]
+  float* partials;         // [grid][2][32]: a CTA's first and last tile row when other CTAs share them
 };
 
 // Lane-wise transpose-reduce of 8 values over the 8 lanes selected by masks
@@ -87,8 +89,8 @@ __device__ __forceinline__ float transpose_reduce8(float v[8], int lane, int m2,
   return keep + __shfl_xor_sync(0xffffffffu, send, m0);
 }
 
-// worker that holds chunk c: the largest w with floor(T*w/W) <= c
-__device__ __forceinline__ int64_t worker_of(int64_t c, int64_t T, int64_t W) { return ((c + 1) * W - 1) / T; }
+// CTA that holds chunk c: the largest b with floor(T*b/G) <= c
+__device__ __forceinline__ int64_t cta_of(int64_t c, int64_t T, int64_t G) { return ((c + 1) * G - 1) / T; }
 
 template <class GemvArgs>
 __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, float v) {
@@ -96,90 +98,104 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
   else static_cast<uint16_t*>(y)[n] = f32_to_bf16_bits(v);
 }
 
-// Finish the segment (item it, tile row tr) of worker wk, whose range starts
-// at lo: `val` is the lane's sum for row `row` of the tile row.
+// A tile row shared with other CTAs: park this CTA's sum (lane = row) in slot
+// `slot`; the last CTA to arrive adds the slots in CTA order and stores y.
 template <class GemvArgs>
-__device__ __noinline__ void flush_segment(const GemvArgs& a, int64_t wk, int64_t lo, int64_t hi, int it, int64_t tr,
-                                           int row, float val, int lane) {
+__device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int slot, int it, int64_t tr, float val,
+                                           int lane) {
   const GemvItemDev& item = a.items[it];
   const int64_t row_lo = item.cbase + tr * item.TC, row_hi = row_lo + item.TC;
-  const int64_t n = tr * 32 + row;
-  if (lo <= row_lo && row_hi <= hi) {               // the whole tile row is ours
-    store_y(a, item.y, n, val);
-    return;
-  }
-  const int slot = (lo >= row_lo) ? 0 : 1;          // a worker's first segment uses slot 0
-  a.partials[(wk * 2 + slot) * 32 + row] = val;
+  a.partials[(b * 2 + slot) * 32 + lane] = val;
   __threadfence();
   __syncwarp();
-  const int64_t w_first = worker_of(row_lo, a.T, a.workers);
-  const int64_t w_last = worker_of(row_hi - 1, a.T, a.workers);
+  const int64_t c_first = cta_of(row_lo, a.T, a.grid), c_last = cta_of(row_hi - 1, a.T, a.grid);
   uint32_t* counter = &a.counters[item.trbase + tr];
   uint32_t old = 0;
   if (lane == 0) old = atomicAdd(counter, 1u);
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != static_cast<uint32_t>(w_last - w_first)) return;   // not the last to arrive
+  if (old != static_cast<uint32_t>(c_last - c_first)) return;   // not the last to arrive
   __threadfence();
   float sum = 0.f;
-  for (int64_t w = w_first; w <= w_last; ++w) {
-    const int64_t wlo = (a.T * w) / a.workers;
-    float* p = &a.partials[(w * 2 + ((wlo >= row_lo) ? 0 : 1)) * 32 + row];
+  for (int64_t c = c_first; c <= c_last; ++c) {
+    const int64_t clo = (a.T * c) / a.grid;
+    float* p = &a.partials[(c * 2 + ((clo >= row_lo) ? 0 : 1)) * 32 + lane];
     sum += ld_cg_f32(p);
     *p = 0.f;                                       // leave the workspace zero-filled
   }
-  store_y(a, item.y, n, sum);
+  store_y(a, item.y, tr * 32 + lane, sum);
   __syncwarp();
   if (lane == 0) *counter = 0u;
 }
 
 // ------------------------------------------------------- chunk bodies ----
 
-// q4: sum over one 16-byte run (32 codes of group g, one row) of v * x with
-// v = 1 + c 2^-8 (even k) / 1 + c 2^-4 (odd k); xv are (even, odd) x pairs.
-__device__ __forceinline__ float2 q4_run(uint4 cw, const float2 (&xv)[16]) {
-  const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-  const uint32_t ONE = 0x3F800000u;
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t a = w[t] << 15, b = w[t] << 7, c = w[t] >> 1, d = w[t] >> 9;
-    const float2 v0 = make_float2(__uint_as_float(lop3_and_or(a, 0x00078000u, ONE)),
-                                  __uint_as_float(lop3_and_or(a, 0x00780000u, ONE)));
-    const float2 v1 = make_float2(__uint_as_float(lop3_and_or(b, 0x00078000u, ONE)),
-                                  __uint_as_float(lop3_and_or(b, 0x00780000u, ONE)));
-    const float2 v2 = make_float2(__uint_as_float(lop3_and_or(c, 0x00078000u, ONE)),
-                                  __uint_as_float(lop3_and_or(c, 0x00780000u, ONE)));
-    const float2 v3 = make_float2(__uint_as_float(lop3_and_or(d, 0x00078000u, ONE)),
-                                  __uint_as_float(lop3_and_or(d, 0x00780000u, ONE)));
-    acc0 = ffma2(v0, xv[4 * t + 0], acc0);
-    acc1 = ffma2(v1, xv[4 * t + 1], acc1);
-    acc0 = ffma2(v2, xv[4 * t + 2], acc0);
-    acc1 = ffma2(v3, xv[4 * t + 3], acc1);
-  }
-  return fadd2(acc0, acc1);
+// q4 kinds.  Per chunk, the warp first turns the 256-wide bf16 x slice into
+// 16-bit fixed point per 32-column group: q_k = round(x_k 2^(141 - E_g)),
+// E_g the biased exponent of max |x| over the group, so |q_k| <= 255 * 128
+// (a bf16 has 8 significant bits) and the rounding error is at most 2^-16 of
+// the group's largest |x|.  q = 256 P1 + P0 is kept as two byte planes (P0
+// unsigned, P1 signed), packed four columns to a word in the order dp4a meets
+// the codes: low nibbles (even k) and high nibbles (odd k) of a code word.
+// Then for each (row, group) the code dot product is exact integer work:
+//   S0 = sum c P0, S1 = sum c P1 (dp4a, 4 codes per instruction),
+//   sum_k c_k x_k = (256 S1 + S0) 2^(E_g - 141)
+// and y_r += s_rg (sum_k c_k x_k) + z_rg X_g with X_g = sum_k x_k in fp32.
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 template <int KIND>
-__device__ __forceinline__ void q4_chunk(uint32_t st, int lane, float (&yacc)[8]) {
+__device__ __forceinline__ void q4_chunk(uint32_t st, uint32_t scratch, int lane, float (&yacc)[8]) {
   constexpr int CB = chunk_bytes_of(KIND);
-  const int q = lane >> 3, g = lane & 7;
-  // x of group g: 32 bf16 = 16 (even, odd) pairs
-  float2 xv[16];
-  float2 xs = make_float2(0.f, 0.f);
+  // ---- x slice -> byte planes.  Prep lane (gp = lane & 7, tp = lane >> 3) owns the
+  // 8 columns gp*32 + 8tp .. +7 of the slice, i.e. code word tp of group gp.
+  const int gp = lane & 7, tp = lane >> 3;
+  const uint4 xr = lds128(st + CB + gp * 64 + tp * 16);
+  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+  uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
+                         __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
+  uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const int E = max(static_cast<int>(mx >> 7), 15);             // biased exponent of the group's max |x|
+  const float scale = __int_as_float((268 - E) << 23);          // 2^(141 - E)
+  const float inv = __int_as_float((E - 14) << 23);             // 2^(E - 141)
+  float xs = 0.f;
+  int q[8];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const uint4 xr = lds128(st + CB + g * 64 + u * 16);
-    const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      xv[4 * u + j] = make_float2(__uint_as_float(xw[j] << 16), __uint_as_float(xw[j] & 0xFFFF0000u));
-      xs = fadd2(xs, xv[4 * u + j]);
-    }
+  for (int j = 0; j < 4; ++j) {
+    const float f0 = __uint_as_float(xw[j] << 16), f1 = __uint_as_float(xw[j] & 0xFFFF0000u);
+    xs += f0 + f1;
+    q[2 * j] = __float_as_int(fmaf(f0, scale, 12582912.0f)) - 0x4B400000;       // round to nearest
+    q[2 * j + 1] = __float_as_int(fmaf(f1, scale, 12582912.0f)) - 0x4B400000;
   }
-  const float xsum = xs.x + xs.y;
+  xs += __shfl_xor_sync(0xffffffffu, xs, 8);
+  xs += __shfl_xor_sync(0xffffffffu, xs, 16);                   // X_g for g = lane & 7
+  const uint32_t p0e = prmt(prmt(q[0], q[2], 0x0040), prmt(q[4], q[6], 0x0040), 0x5410);
+  const uint32_t p0o = prmt(prmt(q[1], q[3], 0x0040), prmt(q[5], q[7], 0x0040), 0x5410);
+  const uint32_t p1e = prmt(prmt(q[0], q[2], 0x0051), prmt(q[4], q[6], 0x0051), 0x5410);
+  const uint32_t p1o = prmt(prmt(q[1], q[3], 0x0051), prmt(q[5], q[7], 0x0051), 0x5410);
+  // planes of (group gp, word tp) at [tp][gp]: conflict-free both ways
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(p0e), "r"(p0o),
+               "r"(p1e), "r"(p1o)
+               : "memory");
+  __syncwarp();
+  // ---- decode lane (q = lane >> 3, g = lane & 7): rows 4i + q of group g
+  const int qr = lane >> 3, g = lane & 7;
+  uint4 P[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) P[t] = lds128(scratch + (t * 8 + g) * 16);
+  __syncwarp();                                                 // scratch is rewritten by the next chunk
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + q;
+    const int r = 4 * i + qr;
     const uint4 cw = lds128(st + r * 128 + g * 16);
     float s, z;
     if constexpr (KIND == kQ4_1) {
@@ -191,9 +207,19 @@ __device__ __forceinline__ void q4_chunk(uint32_t st, int lane, float (&yacc)[8]
       s = S * static_cast<float>(lds_u8(st + kQ4KSc + r * 8 + g));
       z = M * static_cast<float>(lds_u8(st + kQ4KMn + r * 8 + g));
     }
-    const float2 acc = q4_run(cw, xv);
-    const float dot = fmaf(acc.x - xs.x, 256.f, (acc.y - xs.y) * 16.f);
-    yacc[i] = fmaf(s, dot, fmaf(z, xsum, yacc[i]));
+    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    uint32_t s0 = 0;
+    int s1 = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t lo = w[t] & 0x0F0F0F0Fu, hi = (w[t] >> 4) & 0x0F0F0F0Fu;
+      s0 = dp4a_uu(lo, P[t].x, s0);
+      s0 = dp4a_uu(hi, P[t].y, s0);
+      s1 = dp4a_us(lo, P[t].z, s1);
+      s1 = dp4a_us(hi, P[t].w, s1);
+    }
+    const float dot = __int2float_rn(s1 * 256 + static_cast<int>(s0));   // exact: |.| < 2^24
+    yacc[i] = fmaf(s * inv, dot, fmaf(z, xs, yacc[i]));
   }
 }
 
@@ -288,13 +314,76 @@ struct Pos {
   }
 };
 
+// ----------------------------------------------------- segment results ----
+
+// Range of warp w of a CTA owning chunks [Lc, Hc) split over nw warps.
+__device__ __forceinline__ int64_t warp_lo(int64_t Lc, int64_t Hc, int w, int nw) { return Lc + ((Hc - Lc) * w) / nw; }
+
+// End of a segment (item it, tile row tr) of a warp with range [lo, hi):
+// store y if the warp holds the whole tile row, else park the row sums in the
+// warp's slot (0 for its first segment, 1 for its last).
+template <class GemvArgs>
+__device__ __forceinline__ void park_segment(const GemvArgs& a, int64_t lo, int64_t hi, int it, int64_t tr, bool first,
+                                             int row, float val, float* wslots) {
+  const GemvItemDev& item = a.items[it];
+  const int64_t row_lo = item.cbase + tr * item.TC, row_hi = row_lo + item.TC;
+  if (lo <= row_lo && row_hi <= hi) {
+    store_y(a, item.y, tr * 32 + row, val);
+    return;
+  }
+  wslots[(first ? 0 : 32) + row] = val;
+}
+
+// Item and tile row of chunk c (c inside the batch).
+template <class GemvArgs>
+__device__ __forceinline__ void row_of(const GemvArgs& a, int64_t c, int& it, int64_t& tr, int64_t& r0, int64_t& r1) {
+  int lo = 0, hi = a.nitems - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
+  }
+  it = lo;
+  const GemvItemDev& item = a.items[it];
+  tr = (c - item.cbase) / item.TC;
+  r0 = item.cbase + tr * item.TC;
+  r1 = r0 + item.TC;
+}
+
+// After the CTA barrier: every tile row split between warps of this CTA is
+// finished by the warp holding its first chunk in the CTA (warp order sum);
+// rows that also reach into other CTAs continue with cross_cta_row.
+template <class GemvArgs>
+__device__ __forceinline__ void combine_rows(const GemvArgs& a, int64_t b, int64_t Lc, int64_t Hc, int w, int nw,
+                                             int64_t lo, int64_t hi, const float* slots, int lane) {
+  for (int k = 0; k < 2; ++k) {
+    // k = 0: the row holding lo (the warp's first row); k = 1: the row holding hi - 1 (its last)
+    int it;
+    int64_t tr, r0, r1;
+    row_of(a, k == 0 ? lo : hi - 1, it, tr, r0, r1);
+    if (k == 1 && r0 <= lo) break;                             // last row == first row
+    if (r0 >= lo && r1 <= hi) continue;                         // whole row inside this warp: already stored
+    const bool owner = (k == 1) || r0 >= lo || w == 0;          // holds the row's first chunk in this CTA
+    if (!owner) continue;
+    float sum = slots[w * 64 + (k == 0 ? 0 : 32) + lane];
+    for (int v = w + 1; v < nw; ++v) {                          // later warps whose first row is this row
+      if (warp_lo(Lc, Hc, v, nw) >= r1) break;
+      sum += slots[v * 64 + lane];
+    }
+    if (r0 >= Lc && r1 <= Hc) store_y(a, a.items[it].y, tr * 32 + lane, sum);
+    else cross_cta_row(a, b, (Lc >= r0) ? 0 : 1, it, tr, sum, lane);
+  }
+}
+
 template <int KIND, class GemvArgs>
-__device__ __forceinline__ void issue_stage(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
+__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  const GemvItemDev& item = a.items[p.it];
   mbar_arrive_expect_tx(bar, CB + kXSliceBytes);
-  bulk_g2s(dst, item.chunks + p.local * CB, CB, bar);
-  bulk_g2s(dst + CB, item.x + static_cast<int64_t>(p.tc) * kXSliceBytes, kXSliceBytes, bar);
+  bulk_g2s(dst, a.items[p.it].chunks + p.local * CB, CB, bar);
+}
+template <int KIND, class GemvArgs>
+__device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
+  constexpr int CB = chunk_bytes_of(KIND);
+  bulk_g2s(dst + CB, a.items[p.it].x + static_cast<int64_t>(p.tc) * kXSliceBytes, kXSliceBytes, bar);
 }
 
 template <int KIND, int MAXB>
@@ -302,14 +391,19 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int SB = chunk_bytes_of(KIND) + kXSliceBytes;     // stage bytes
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int64_t wk = static_cast<int64_t>(blockIdx.x) * nwarps + warp;
-  if (wk >= a.workers) return;                                 // idle warp of the last CTA
-  const int64_t lo = (a.T * wk) / a.workers, hi = (a.T * (wk + 1)) / a.workers;
+  const int64_t b = blockIdx.x;
+  const int64_t Lc = (a.T * b) / a.grid, Hc = (a.T * (b + 1)) / a.grid;
+  const int64_t lo = Lc + ((Hc - Lc) * warp) / nwarps, hi = Lc + ((Hc - Lc) * (warp + 1)) / nwarps;
   const int stages = a.stages;
+  const uint64_t ring_bytes = static_cast<uint64_t>(nwarps) * stages * SB;
   uint8_t* ring = smem + static_cast<uint64_t>(warp) * stages * SB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<uint64_t>(nwarps) * stages * SB) + warp * stages;
-  const int n = static_cast<int>(hi - lo);                     // chunks of this worker
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * stages;
+  uint8_t* tail = smem + ring_bytes + align16(static_cast<uint64_t>(nwarps) * stages * 8);
+  const uint32_t scratch = smem_u32(tail) + warp * kScratchBytes;
+  float* slots = reinterpret_cast<float*>(tail + nwarps * kScratchBytes);   // [nwarps][2][32]
+  const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur, pre;                             // chunk being processed / next chunk to fetch
   cur.seek(a, lo);
@@ -317,8 +411,17 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
+    // weights never change between launches: fetch the first chunks before waiting on the previous grid
+    Pos p = pre;
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_stage<KIND>(a, pre, ring + s * SB, &bars[s]);
+      issue_chunk<KIND>(a, p, ring + s * SB, &bars[s]);
+      p.next(a);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
+  if (lane == 0) {
+    for (int s = 0; s < stages && s < n; ++s) {
+      issue_xslice<KIND>(a, pre, ring + s * SB, &bars[s]);
       pre.next(a);
     }
   }
@@ -328,41 +431,49 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
 #pragma unroll
   for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
   int seg_it = cur.it, seg_tr = cur.tr;
+  bool seg_first = true;
   uint32_t phase = 0;                       // bit s: parity awaited next on stage s
   int s = 0;
+  bool failed = false;
 
   for (int j = 0; j < n; ++j) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (phase >> s) & 1u));
-    if (!ok) {
-      // A wait gave up: record it, let this worker's copies in flight land, stop.
-      if (lane == 0) atomicOr(a.err, 1u);
-      for (int t = 0; t < stages; ++t) mbar_wait_bounded(&bars[t], (phase >> t) & 1u, 100000000ull);
-      return;
-    }
+    if (!ok) { failed = true; break; }
     phase ^= 1u << s;
     if (cur.it != seg_it || cur.tr != seg_tr) {    // the previous segment is complete
       int row;
       const float v = finish_rows<KIND>(yacc, lane, row);
-      flush_segment(a, wk, lo, hi, seg_it, seg_tr, row, v, lane);
+      park_segment(a, lo, hi, seg_it, seg_tr, seg_first, row, v, slots + warp * 64);
 #pragma unroll
       for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
       seg_it = cur.it;
       seg_tr = cur.tr;
+      seg_first = false;
     }
     const uint32_t st = smem_u32(ring + s * SB);
-    if constexpr (Q4) q4_chunk<KIND>(st, lane, yacc);
+    if constexpr (Q4) q4_chunk<KIND>(st, scratch, lane, yacc);
     else q8_chunk<KIND>(st, lane, yacc);
     __syncwarp();
     if (lane == 0 && j + stages < n) {
-      issue_stage<KIND>(a, pre, ring + s * SB, &bars[s]);
+      issue_chunk<KIND>(a, pre, ring + s * SB, &bars[s]);
+      issue_xslice<KIND>(a, pre, ring + s * SB, &bars[s]);
       pre.next(a);
     }
     cur.next(a);
     if (++s == stages) s = 0;
   }
-  int row;
-  const float v = finish_rows<KIND>(yacc, lane, row);
-  flush_segment(a, wk, lo, hi, seg_it, seg_tr, row, v, lane);
+  if (failed) {
+    // A wait gave up: record it and let this warp's copies in flight land.
+    if (lane == 0) atomicOr(a.err, 1u);
+    for (int t = 0; t < stages; ++t) mbar_wait_bounded(&bars[t], (phase >> t) & 1u, 100000000ull);
+  } else {
+    int row;
+    const float v = finish_rows<KIND>(yacc, lane, row);
+    park_segment(a, lo, hi, seg_it, seg_tr, seg_first, row, v, slots + warp * 64);
+  }
+  __syncwarp();
+  __syncthreads();
+  if (!failed) combine_rows(a, b, Lc, Hc, warp, nwarps, lo, hi, slots, lane);
 }
 
 // ----------------------------------------------------------------- host ----
@@ -372,33 +483,34 @@ bool gemv_plan(int kind, int64_t T, int sms, int max_smem, GemvPlan* p) {
   if (CB == 0 || sms <= 0 || T <= 0) return false;
   const uint64_t SB = static_cast<uint64_t>(CB) + kXSliceBytes;
   static const int kWarpChoices[] = {16, 12, 8, 6, 4, 2, 1};
+  auto need = [&](int w, int st) {
+    return static_cast<uint64_t>(w) * st * SB + align16(static_cast<uint64_t>(w) * st * 8) +
+           static_cast<uint64_t>(w) * (kScratchBytes + kSlotBytes);
+  };
   int warps = 0, stages = 0;
   for (int w : kWarpChoices) {
-    const uint64_t need = static_cast<uint64_t>(w) * 2 * (SB + 8);
-    if (need <= static_cast<uint64_t>(max_smem)) { warps = w; stages = 2; break; }
+    if (need(w, 2) <= static_cast<uint64_t>(max_smem)) { warps = w; stages = 2; break; }
   }
   if (!warps) return false;
-  if (static_cast<uint64_t>(warps) * 3 * (SB + 8) <= static_cast<uint64_t>(max_smem)) stages = 3;
-  // Small problems: spread chunks over SMs before stacking warps.
-  const int64_t per_sm = (T + sms - 1) / sms;
-  if (per_sm < warps) warps = static_cast<int>(per_sm < 1 ? 1 : per_sm);
-  int64_t grid = (T + warps - 1) / warps;
+  if (need(warps, 3) <= static_cast<uint64_t>(max_smem)) stages = 3;
+  // One CTA per SM; small problems use fewer CTAs of at least ~4 chunks each so
+  // that split tile rows are combined inside a CTA rather than across CTAs.
+  int64_t grid = T / 4;
+  if (grid < 1) grid = 1;
   if (grid > sms) grid = sms;
-  int64_t workers = grid * warps;
-  if (workers > T) workers = T;                    // every worker gets at least one chunk
-  if (workers > kMaxWorkers) workers = kMaxWorkers;
-  grid = (workers + warps - 1) / warps;
+  if (grid > kMaxCtas) grid = kMaxCtas;
+  const int64_t per_cta = T / grid;                // every warp gets at least one chunk
+  if (per_cta < warps) warps = static_cast<int>(per_cta);
   p->warps = warps;
   p->stages = stages;
   p->grid = static_cast<int>(grid);
-  p->workers = static_cast<int>(workers);
-  p->smem = static_cast<uint64_t>(warps) * stages * (SB + 8);
+  p->smem = need(warps, stages);
   return true;
 }
 
 uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks) {
-  const int64_t w = total_chunks < kMaxWorkers ? total_chunks : kMaxWorkers;
-  return kWsErrBytes + align16(static_cast<uint64_t>(total_tile_rows) * 4) + static_cast<uint64_t>(w) * 2 * 32 * 4;
+  (void)total_chunks;
+  return kWsErrBytes + align16(static_cast<uint64_t>(total_tile_rows) * 4) + static_cast<uint64_t>(kMaxCtas) * 2 * 32 * 4;
 }
 
 template <int KIND, int MAXB>
@@ -406,7 +518,21 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
   const int slot = KIND + (MAXB == 1 ? 0 : MAXB == 8 ? 4 : 8);
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB>), slot);
   if (e != cudaSuccess) return e;
-  gemv_kernel<KIND, MAXB><<<p.grid, p.warps * 32, p.smem, s>>>(a);
+  // Programmatic dependent launch: SMs freed by the previous grid start this
+  // one at once; the kernel waits for the previous grid before touching x, y
+  // or the workspace.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.warps * 32);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -430,7 +556,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   if (!gemv_plan(kind, T, sms, max_smem, &p)) return cudaErrorInvalidValue;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.nitems = n;
-  a.workers = p.workers;
+  a.grid = p.grid;
   a.stages = p.stages;
   a.out_f32 = out_f32;
   a.T = T;

@@ -27,10 +27,9 @@ struct GemvItem {
   int64_t TR, TC;
 };
 struct GemvPlan {
-  int warps = 0;       // warp workers per CTA
+  int warps = 0;       // warps per CTA, each owning a contiguous part of the CTA's chunks
   int stages = 0;      // ring stages per warp
-  int grid = 0;        // CTAs
-  int workers = 0;     // warp workers in the grid, <= chunks
+  int grid = 0;        // CTAs, each owning a contiguous range of chunks
   size_t smem = 0;     // dynamic shared memory bytes
 };
 bool gemv_plan(int kind, int64_t total_chunks, int sms, int max_smem, GemvPlan* plan);
@@ -55,7 +54,7 @@ cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, co
 
 // Workspace layout shared by the GEMV launcher and kernel.
 constexpr uint64_t kWsErrBytes = 16;              // error word (+ padding)
-constexpr int kMaxWorkers = 4096;                 // upper bound of warp workers per launch
+constexpr int kMaxCtas = 1024;                    // upper bound of CTAs per GEMV launch
 __host__ __device__ inline uint64_t align16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
 
 }  // namespace q4nx
