@@ -75,6 +75,8 @@ def _load():
         "q4nx_repack_q4k": ([P, U64, I64, I64, P, U64, P], I),
         "q4nx_argmax": ([P, I, I64, P, P], I),
         "q4nx_check": ([P, P], I),
+        "q4nx_gemv_noalloc": ([W, P, P, I, P], I),
+        "q4nx_noalloc_scratch_bytes": ([], U64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -86,7 +88,7 @@ def _load():
 lib = _load()
 EXPORTS = ("q4nx_chunk_bytes", "q4nx_status_str", "q4nx_abi_version", "q4nx_decode", "q4nx_gemv",
            "q4nx_gemv_workspace", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_argmax",
-           "q4nx_check")
+           "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes")
 
 
 def q4nx_chunk_bytes(kind: int) -> int:
@@ -228,6 +230,23 @@ def q4nx_gemv_batch(items, out_dtype="bf16", ws: torch.Tensor | None = None):
     with torch.cuda.device(items[0][0].device):
         GemvBatch(items, out_dtype, ws)()
     return [y for _, _, y in items]
+
+
+def q4nx_gemv_noalloc(w: Weight, x: torch.Tensor, out: torch.Tensor | None = None, out_dtype="bf16") -> torch.Tensor:
+    """q4nx_gemv with the library's built-in scratch: allocates nothing on the device
+    (the output tensor, when not given, is the only allocation, made here by torch)."""
+    _cuda(w.chunks, "chunks")
+    _cuda(x, "x")
+    code = _out_code(out_dtype)
+    with torch.cuda.device(w.device):
+        if out is None:
+            out = torch.empty(w.rows, dtype=torch.bfloat16 if code == Q4NX_OUT_BF16 else torch.float32,
+                              device=w.device)
+        _cuda(out, "out")
+        cw = w.c()
+        _check(lib.q4nx_gemv_noalloc(ctypes.byref(cw), x.data_ptr(), out.data_ptr(), code, _stream(w.device)),
+               "q4nx_gemv_noalloc")
+    return out
 
 
 def q4nx_gemm_m64(w: Weight, X: torch.Tensor, out: torch.Tensor | None = None, out_dtype="bf16",

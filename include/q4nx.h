@@ -151,6 +151,27 @@ int q4nx_repack_q4k(const void* in_dev, uint64_t in_bytes, int64_t rows, int64_t
  * the first NaN wins; +0 and -0 are equal.  1 <= M <= 65535, 1 <= V < 2^31. */
 int q4nx_argmax(const float* logits_dev, int M, int64_t V, int32_t* idx_dev, void* stream);
 
+/* GEMV without any allocation, for callers that may not allocate device memory
+ * at all: code that runs under a strict no-allocation policy once set up (for
+ * example a real-time decode loop, or a plug-in inside a framework that owns
+ * every device allocation and hands out only inputs and outputs).  The pages
+ * have no counterpart of this entry point; it is q4nx_gemv with its scratch
+ * memory (error word, per-tile-row counters, partial sums) taken from a 1 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * keeps until the process exits.
+ * The caller passes inputs and outputs only, exactly as for q4nx_gemv.
+ * The first call on each device looks up that device's copy of the array
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call clears the counters it uses, so a call never depends on what an
+ * earlier call left behind; but all calls on a device share the one array, so
+ * calls that can overlap on the GPU (different streams, or concurrent graph
+ * branches) race and must be serialised by the caller.
+ * Returns Q4NX_E_WORKSPACE if the weight needs more scratch than the array
+ * holds (q4nx_noalloc_scratch_bytes(); tile rows beyond about 196 000);
+ * otherwise the statuses of q4nx_gemv.  Calls no cudaMalloc or cudaFree. */
+int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype, void* stream);
+uint64_t q4nx_noalloc_scratch_bytes(void);
+
 /* Read and clear the error word of a workspace (synchronises `stream`).
  * Returns Q4NX_OK, or Q4NX_E_DEVICE_TIMEOUT if a bounded in-kernel wait of a
  * call that used this workspace gave up (its outputs are then invalid). */

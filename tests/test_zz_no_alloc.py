@@ -1,0 +1,81 @@
+"""q4nx_gemv_noalloc: the GEMV for callers that may not allocate device memory.
+
+Some callers (a decode loop under a no-allocation policy once it is set up, a
+plug-in whose host framework owns every device allocation) can pass inputs and
+outputs but cannot hand the library a scratch buffer.  This entry point uses
+scratch compiled into the library instead.  The test calls it through the C ABI
+twice in a row (the second call runs on whatever the first left in the shared
+scratch) and checks both results against q4nx_gemv, the entry point that takes
+a caller-owned workspace, within the tolerance of the other GPU tests.
+
+This file is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def q():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build()
+    import dequant_gemv_gb300
+
+    return dequant_gemv_gb300
+
+
+def _dev_bytes(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("kind,N,K,out", [
+    (synth.Q4_1, 4096, 12288, "bf16"),      # tile rows shared between CTAs
+    (synth.Q4_1, 1024, 1024, "f32"),
+    (synth.Q4_K, 2560, 9728, "bf16"),
+    (synth.Q8_BLK, 8192, 2560, "f32"),
+])
+def test_noalloc_matches_workspace_entry_point(q, kind, N, K, out):
+    f, w = synth.make(kind, N, K, synth.rng(11, 0, N + K))
+    x = synth.activations(synth.rng(11, 1, N + K), 1, K)[0]
+    W = q.Weight(_dev_bytes(w), kind, N, K)
+    xd = _dev_bf16(x)
+    ref = q.q4nx_gemv(W, xd, out_dtype=out).float().cpu().numpy().astype(np.float64)
+    code = q.Q4NX_OUT_F32 if out == "f32" else q.Q4NX_OUT_BF16
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    cw = W.c()
+    stream = torch.cuda.current_stream().cuda_stream
+    rows = np.arange(0, N, max(1, N // 2048))
+    _, A = oracle.matmul(w, kind, N, K, x, rows=rows)
+    tol = 1e-3 * A + (2.0 ** -8 * np.abs(ref[rows]) if out == "bf16" else 0.0)
+    for call in range(2):
+        y = torch.full((N,), float("nan"), dtype=dt, device=DEV)
+        st = q.lib.q4nx_gemv_noalloc(ctypes.byref(cw), xd.data_ptr(), y.data_ptr(), code, stream)
+        assert st == 0, q.q4nx_status_str(st)
+        got = y.float().cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all(), f"call {call}: output not fully written"
+        assert np.all(np.abs(got[rows] - ref[rows]) <= tol), f"call {call}"
+
+
+def test_noalloc_rejects_more_tile_rows_than_its_scratch(q):
+    cap = int(q.lib.q4nx_noalloc_scratch_bytes())
+    assert cap == 1 << 20
+    t = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    rows = 32 * 300000                               # 300 000 tile rows: more than 1 MiB of counters
+    cw = q.q4nx_weight(t.data_ptr(), 1 << 62, synth.Q4_1, 0, rows, 256)
+    st = q.lib.q4nx_gemv_noalloc(ctypes.byref(cw), t.data_ptr(), t.data_ptr(), 0, None)
+    assert st == 7, q.q4nx_status_str(st)           # Q4NX_E_WORKSPACE, nothing launched
