@@ -39,7 +39,7 @@ namespace q4nx {
 
 constexpr int kXSliceBytes = 512;            // bf16 x of one tile column
 constexpr int kScratchBytes = 512;           // per warp: x byte planes of one chunk
-constexpr int kSlotBytes = 2 * 32 * 4;       // per warp: sums of its first and last tile row
+constexpr int kSlotBytes = 2 * 32 * 4 + 8;   // per warp: sums of its first and last tile row, 2 counters
 constexpr int kMaxBatch = kMaxGemvItems;
 
 struct GemvItemDev {
@@ -98,27 +98,51 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
   else static_cast<uint16_t*>(y)[n] = f32_to_bf16_bits(v);
 }
 
-// A tile row shared with other CTAs: park this CTA's sum (lane = row) in slot
-// `slot`; the last CTA to arrive adds the slots in CTA order and stores y.
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A tile row [r0, r1) shared with other CTAs, after this CTA's warps have
+// combined their parts (lane = row, `val` = this CTA's sum).  The CTA holding
+// the row's first chunk finishes it: it reaches its part last (at the end of
+// its range), so the others have usually posted theirs long before.  The
+// others post their sum in their slot 0 and count themselves in with a
+// release reduction; the finisher waits (bounded) for the count, adds the
+// posted sums in CTA order after its own, stores y and clears what it used.
 template <class GemvArgs>
-__device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int slot, int it, int64_t tr, float val,
-                                           int lane) {
+__device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t Lc, int it, int64_t tr, int64_t r0,
+                                           int64_t r1, float val, int lane) {
   const GemvItemDev& item = a.items[it];
-  const int64_t row_lo = item.cbase + tr * item.TC, row_hi = row_lo + item.TC;
-  a.partials[(b * 2 + slot) * 32 + lane] = val;
-  __threadfence();
-  __syncwarp();
-  const int64_t c_first = cta_of(row_lo, a.T, a.grid), c_last = cta_of(row_hi - 1, a.T, a.grid);
   uint32_t* counter = &a.counters[item.trbase + tr];
-  uint32_t old = 0;
-  if (lane == 0) old = atomicAdd(counter, 1u);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != static_cast<uint32_t>(c_last - c_first)) return;   // not the last to arrive
-  __threadfence();
-  float sum = 0.f;
-  for (int64_t c = c_first; c <= c_last; ++c) {
-    const int64_t clo = (a.T * c) / a.grid;
-    float* p = &a.partials[(c * 2 + ((clo >= row_lo) ? 0 : 1)) * 32 + lane];
+  if (r0 < Lc) {                                      // not the finisher: post
+    a.partials[(b * 2) * 32 + lane] = val;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_add(counter, 1u);
+    return;
+  }
+  const int64_t c_last = cta_of(r1 - 1, a.T, a.grid);
+  const uint32_t expect = static_cast<uint32_t>(c_last - b);
+  uint32_t ok = 1;
+  if (lane == 0) {
+    if (ld_acquire_u32(counter) != expect) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(counter) != expect) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) { ok = 0; atomicOr(a.err, 1u); break; }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return;
+  __syncwarp();
+  float sum = val;
+  for (int64_t c = b + 1; c <= c_last; ++c) {
+    float* p = &a.partials[(c * 2) * 32 + lane];
     sum += ld_cg_f32(p);
     *p = 0.f;                                       // leave the workspace zero-filled
   }
@@ -316,62 +340,45 @@ struct Pos {
 
 // ----------------------------------------------------- segment results ----
 
-// Range of warp w of a CTA owning chunks [Lc, Hc) split over nw warps.
-__device__ __forceinline__ int64_t warp_lo(int64_t Lc, int64_t Hc, int w, int nw) { return Lc + ((Hc - Lc) * w) / nw; }
+// Warp of a CTA owning chunks [Lc, Hc) split over nw warps that holds chunk c.
+__device__ __forceinline__ int warp_of(int64_t c, int64_t Lc, int64_t Hc, int nw) {
+  return static_cast<int>(((c - Lc + 1) * nw - 1) / (Hc - Lc));
+}
 
-// End of a segment (item it, tile row tr) of a warp with range [lo, hi):
-// store y if the warp holds the whole tile row, else park the row sums in the
-// warp's slot (0 for its first segment, 1 for its last).
+// End of a segment (item it, tile row tr) of warp w (range [lo, hi)); each
+// lane holds the sum of the row `row`.  A row held by this warp alone is
+// stored at once.  A row shared with other warps of the CTA is parked in the
+// warp's slot (0: its first segment, 1: its last); the last of those warps to
+// arrive (shared-memory counter of the row's first warp) adds the slots in
+// warp order and stores y, or hands the row on to cross_cta_row when other
+// CTAs share it too.
 template <class GemvArgs>
-__device__ __forceinline__ void park_segment(const GemvArgs& a, int64_t lo, int64_t hi, int it, int64_t tr, bool first,
-                                             int row, float val, float* wslots) {
+__device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_t Lc, int64_t Hc, int w, int nw,
+                                            int64_t lo, int64_t hi, int it, int64_t tr, int row, float val, float* slots,
+                                            uint32_t* cnt, int lane) {
   const GemvItemDev& item = a.items[it];
-  const int64_t row_lo = item.cbase + tr * item.TC, row_hi = row_lo + item.TC;
-  if (lo <= row_lo && row_hi <= hi) {
+  const int64_t r0 = item.cbase + tr * item.TC, r1 = r0 + item.TC;
+  if (lo <= r0 && r1 <= hi) {
     store_y(a, item.y, tr * 32 + row, val);
     return;
   }
-  wslots[(first ? 0 : 32) + row] = val;
-}
-
-// Item and tile row of chunk c (c inside the batch).
-template <class GemvArgs>
-__device__ __forceinline__ void row_of(const GemvArgs& a, int64_t c, int& it, int64_t& tr, int64_t& r0, int64_t& r1) {
-  int lo = 0, hi = a.nitems - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
-  }
-  it = lo;
-  const GemvItemDev& item = a.items[it];
-  tr = (c - item.cbase) / item.TC;
-  r0 = item.cbase + tr * item.TC;
-  r1 = r0 + item.TC;
-}
-
-// After the CTA barrier: every tile row split between warps of this CTA is
-// finished by the warp holding its first chunk in the CTA (warp order sum);
-// rows that also reach into other CTAs continue with cross_cta_row.
-template <class GemvArgs>
-__device__ __forceinline__ void combine_rows(const GemvArgs& a, int64_t b, int64_t Lc, int64_t Hc, int w, int nw,
-                                             int64_t lo, int64_t hi, const float* slots, int lane) {
-  for (int k = 0; k < 2; ++k) {
-    // k = 0: the row holding lo (the warp's first row); k = 1: the row holding hi - 1 (its last)
-    int it;
-    int64_t tr, r0, r1;
-    row_of(a, k == 0 ? lo : hi - 1, it, tr, r0, r1);
-    if (k == 1 && r0 <= lo) break;                             // last row == first row
-    if (r0 >= lo && r1 <= hi) continue;                         // whole row inside this warp: already stored
-    const bool owner = (k == 1) || r0 >= lo || w == 0;          // holds the row's first chunk in this CTA
-    if (!owner) continue;
-    float sum = slots[w * 64 + (k == 0 ? 0 : 32) + lane];
-    for (int v = w + 1; v < nw; ++v) {                          // later warps whose first row is this row
-      if (warp_lo(Lc, Hc, v, nw) >= r1) break;
-      sum += slots[v * 64 + lane];
-    }
-    if (r0 >= Lc && r1 <= Hc) store_y(a, a.items[it].y, tr * 32 + lane, sum);
-    else cross_cta_row(a, b, (Lc >= r0) ? 0 : 1, it, tr, sum, lane);
-  }
+  const int k = (r0 <= lo) ? 0 : 1;                 // the warp's first segment iff the row holds lo
+  slots[(w * 2 + k) * 32 + row] = val;
+  const int wa = warp_of(r0 > Lc ? r0 : Lc, Lc, Hc, nw);
+  const int wb = warp_of((r1 < Hc ? r1 : Hc) - 1, Lc, Hc, nw);
+  const int64_t lo_a = Lc + ((Hc - Lc) * wa) / nw;
+  const int ka = (r0 <= lo_a) ? 0 : 1;             // the row's slot in its first warp
+  __threadfence_block();
+  __syncwarp();
+  uint32_t old = 0;
+  if (lane == 0) old = atomicAdd(&cnt[wa * 2 + ka], 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != static_cast<uint32_t>(wb - wa)) return;   // another warp of the CTA finishes the row
+  __threadfence_block();
+  float sum = slots[(wa * 2 + ka) * 32 + lane];
+  for (int v = wa + 1; v <= wb; ++v) sum += slots[(v * 2) * 32 + lane];
+  if (r0 >= Lc && r1 <= Hc) store_y(a, item.y, tr * 32 + lane, sum);
+  else cross_cta_row(a, b, Lc, it, tr, r0, r1, sum, lane);
 }
 
 template <int KIND, class GemvArgs>
@@ -403,6 +410,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   uint8_t* tail = smem + ring_bytes + align16(static_cast<uint64_t>(nwarps) * stages * 8);
   const uint32_t scratch = smem_u32(tail) + warp * kScratchBytes;
   float* slots = reinterpret_cast<float*>(tail + nwarps * kScratchBytes);   // [nwarps][2][32]
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(slots + nwarps * 64);         // [nwarps][2]
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur, pre;                             // chunk being processed / next chunk to fetch
@@ -425,13 +433,14 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
       pre.next(a);
     }
   }
+  if (lane < 2) cnt[warp * 2 + lane] = 0u;
   __syncwarp();
+  __syncthreads();                          // the row counters are zero before any warp can count
 
   float yacc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
   int seg_it = cur.it, seg_tr = cur.tr;
-  bool seg_first = true;
   uint32_t phase = 0;                       // bit s: parity awaited next on stage s
   int s = 0;
   bool failed = false;
@@ -443,12 +452,11 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     if (cur.it != seg_it || cur.tr != seg_tr) {    // the previous segment is complete
       int row;
       const float v = finish_rows<KIND>(yacc, lane, row);
-      park_segment(a, lo, hi, seg_it, seg_tr, seg_first, row, v, slots + warp * 64);
+      finish_segment(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
 #pragma unroll
       for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
       seg_it = cur.it;
       seg_tr = cur.tr;
-      seg_first = false;
     }
     const uint32_t st = smem_u32(ring + s * SB);
     if constexpr (Q4) q4_chunk<KIND>(st, scratch, lane, yacc);
@@ -469,11 +477,8 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   } else {
     int row;
     const float v = finish_rows<KIND>(yacc, lane, row);
-    park_segment(a, lo, hi, seg_it, seg_tr, seg_first, row, v, slots + warp * 64);
+    finish_segment(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
   }
-  __syncwarp();
-  __syncthreads();
-  if (!failed) combine_rows(a, b, Lc, Hc, warp, nwarps, lo, hi, slots, lane);
 }
 
 // ----------------------------------------------------------------- host ----
