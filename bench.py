@@ -57,6 +57,26 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _traffic_if_current():
+    """DRAM bytes (read + write) of one GEMV launch from the committed ncu capture,
+    or None when the kernel's source has changed since that capture."""
+    import hashlib
+
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for rel in d.get("source_files", []):
+        p = os.path.join(ROOT, rel)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return d.get("gemv_q4_1_bytes_per_launch") if h.hexdigest() == d.get("source_sha256") else None
+
+
 def _matrices():
     """(layer, matrix_id, N, K) of one step."""
     return [(l, mi, n, k) for l in range(synth.QWEN3_06B_LAYERS) for mi, (_, n, k) in enumerate(synth.QWEN3_06B_LAYER)]
@@ -289,11 +309,7 @@ def run_gpu(args, rank: int, world: int):
     launch_us = ms_per_step * 1e3 / launches_per_step
     achieved = alg_bytes_step / launches_per_step / (launch_us * 1e-6) / 1e9
     peak, peak_kind = _peaks()
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            traffic = json.load(f).get("gemv_q4_1_bytes_per_launch")
+    traffic = _traffic_if_current()
 
     # end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps, 200))
