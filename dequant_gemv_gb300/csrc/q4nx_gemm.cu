@@ -1,31 +1,67 @@
 // q4nx_gemm.cu -- fused decode + GEMM for a block of up to 64 tokens on the
-// 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA), sm_103a.
+// 5th-generation tensor cores (tcgen05, TMEM, TMA), sm_103a.
 //
 //   Y[m][n] = sum_k X[m][k] * w[n][k],   w in q4_1 chunks ("Q4NX chunks"
 //   section of the 1bit engine "NPU engine" page: code*scale + zero).
 //
 // Tile: 128 weight rows (4 tile rows of the chunk grid) x 64 tokens; k-steps
 // of 256 columns (one chunk column).  The weight rows are the MMA's M side and
-// the tokens its N side, so one tcgen05.mma (M=128, N=64, K=16, bf16 x bf16 ->
-// fp32 in TMEM) covers the whole token block.
+// the tokens its N side: one tcgen05.mma (M=128, N=64, K=16, bf16 x bf16 ->
+// fp32) covers the whole token block.
 //
-// Warp roles (23 warps):
+// Data path of one k-step:
+//   4 chunks --TMA--> shared memory --ld.shared--> dequant warps
+//        --tcgen05.st--> TMEM (A operand, bf16, 128 lanes x 128 columns)
+//   X[0:64, k-step] --TMA, 128-byte swizzle--> shared memory (B operand)
+//   tcgen05.mma reads A from TMEM and B from shared memory, accumulates in TMEM.
+// A never touches shared memory: with N = 64, an MMA that read A from shared
+// memory would spend two thirds of the SM's shared-memory bandwidth on A
+// alone, and the TMA fills, the code reads and the B reads need that bandwidth.
+//
+// Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31 only):
 //   warp 0       weight producer: per k-step the 4 chunks' code regions (3-D
-//                tensor copy, 128-byte swizzle) and scale/zero regions (1-D
-//                bulk copies) into one of 4 weight stages;
-//   warp 1       X producer: the 64 x 256 bf16 X slice of the k-step (4 boxes of
-//                64 x 64, 128-byte swizzle) into one of 2 X stages;
-//   warp 2       TMEM allocator and MMA issuer (one thread);
-//   warps 3-18   dequant: warp d decodes tile row d%4, columns 64(d/4)..+63 of
-//                the step, one thread per weight row, into A stage d/4 (bf16,
-//                canonical K-major 128-byte-swizzled layout, 128 x 64);
-//   warps 19-22  epilogue: TMEM -> registers -> Y, or a split-K partial.
-// Two accumulators in TMEM (2 x 64 columns) let the epilogue of one tile
-// overlap the main loop of the next.  Work is spread stream-K style: every CTA
-// owns a contiguous range of (tile, k-step) units; a tile split between CTAs
-// is finished by the last CTA to arrive, which adds the fp32 partials in CTA
-// order (deterministic).  Every wait is bounded; if one gives up, the CTA sets
-// a shared abort flag, records the error in the workspace and winds down.
+//                tensor copy, 128-byte swizzle, so that row-wise 16-byte reads
+//                are free of bank conflicts) and scale/zero regions (1-D bulk
+//                copies) into one of kWStages stages;
+//   warp 1       X producer: the 64 x 256 bf16 slice of X (4 boxes of 64 x 64)
+//                into one of kStages stages;
+//   warp 2       MMA issuer: the whole warp runs the loop (its values stay
+//                warp-uniform) and one elected lane issues each k-step's 16
+//                MMAs and their commit as one block;
+//   warp 3       TMEM allocator;
+//   warps 4-11   dequant: warp w decodes tile row w%4 (the TMEM lanes of that
+//                tile row), columns 128*((w-4)/4) .. +127 of the k-step, one
+//                thread per weight row, into the A half of one of kStages
+//                stages (the A half in TMEM, the X half in shared memory);
+//   warps 12-15  epilogue: TMEM -> registers -> Y, or a split-tile partial.
+// Eight dequant warps rather than sixteen: the MMA warp shares its
+// sub-partition's issue slots with the dequant warps there, and fewer of them
+// let it keep the tensor pipe fed.
+// Two accumulators (2 x 64 TMEM columns) let the epilogue of one tile overlap
+// the main loop of the next.  A stage is filled by 17 arrivals (the X
+// producer's, with the TMA byte count, and the 16 dequant warps') and emptied
+// by one MMA commit, so the MMA thread waits once and commits once per k-step:
+// each wait or commit in that single issuing thread delays the tensor pipe.
+//
+// Work split (stream-K): the (tile, k-step) units are cut into one contiguous
+// range per CTA.  A tile shared by several CTAs is finished by the CTA that
+// holds its first k-step.  That CTA reaches the tile at the end of its range,
+// while the others (which hold the tile's later k-steps at the start of their
+// ranges) post their fp32 partials early; the finisher gathers them into its
+// epilogue warps' registers while its own main loop still runs, then adds
+// them to its accumulator.  The sum order is fixed (the other CTAs' partials in CTA order,
+// then the finisher's own), so results are deterministic.  Every wait is
+// bounded; if one gives up, the CTA records the error in the workspace and
+// winds down.
+//
+// The finisher waits for CTAs of the same launch, so the launch relies on all
+// of its CTAs being resident at once: the grid is at most one CTA per SM, and
+// a CTA needs most of an SM's shared memory.
+//
+// Programmatic dependent launch: the kernel lets the next grid in the stream
+// launch as soon as all of its CTAs are running, and starts its own weight
+// copies before waiting for the previous grid; X, Y and the workspace are
+// touched only after that wait.
 #include <cuda.h>
 
 #include "q4nx_device.cuh"
@@ -35,22 +71,31 @@ namespace q4nx {
 namespace gemm {
 
 constexpr int kTileM = 128, kTileN = 64, kStepK = 256;
-constexpr int kWStages = 4, kXStages = 2, kAStages = 4, kAccs = 2;
+constexpr int kWStages = 6, kStages = 3, kAccs = 2;
 constexpr int kCodes = 4096, kScales = 1024;
 constexpr int kWBytes = 4 * kCodes + 4 * kScales;     // 20 KB: codes (1024-aligned) then scales
 constexpr int kXBox = 64 * 128;                        // 64 tokens x 64 k of bf16
 constexpr int kXBytes = 4 * kXBox;                     // 32 KB
-constexpr int kABytes = 128 * 128;                     // 128 rows x 64 k of bf16
 constexpr int kWOff = 0;
 constexpr int kXOff = kWOff + kWStages * kWBytes;
-constexpr int kAOff = kXOff + kXStages * kXBytes;
-constexpr int kBarOff = kAOff + kAStages * kABytes;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;       // barriers and flags, alignment slack
-constexpr int kDequantWarps = 16;
-constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpDequant0 = 3, kWarpEpi0 = kWarpDequant0 + kDequantWarps;
+constexpr int kBarOff = kXOff + kStages * kXBytes;
+constexpr int kSmemBytes = kBarOff + 512 + 1024;       // barriers and flags, alignment slack
+constexpr int kDequantWarps = 8;
+constexpr int kQuartersPerWarp = 16 / kDequantWarps;   // 64-column quarters of a k-step per dequant warp
+constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpAlloc = 3, kWarpDequant0 = 4;
+constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
 constexpr int kWarps = kWarpEpi0 + 4;
 constexpr int kThreads = kWarps * 32;
-static_assert(kWStages * kWBytes % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions must stay 1024-aligned");
+// TMEM columns: accumulators [0, 128); A stages from 128, 128 columns each
+// (4 quarters of 32 columns; a column holds 2 bf16 of one weight row).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemA = kAccs * kTileN;
+constexpr uint32_t kAStageCols = kStepK / 2;
+static_assert(kTmemA + kStages * kAStageCols <= kTmemCols, "TMEM budget");
+static_assert(kWarpDequant0 % 4 == 0 && kWarpEpi0 % 4 == 0, "TMEM lane quarters follow warp % 4");
+static_assert(kDequantWarps == 8, "dequant warps: two per TMEM lane quarter");
+static_assert(kWBytes % 1024 == 0 && kXOff % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions 1024-aligned");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // tcgen05 instruction descriptor: D fp32, A bf16, B bf16, both K-major, N = 64, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kTileN >> 3) << 17) | ((kTileM >> 4) << 24);
@@ -59,8 +104,8 @@ struct Args {
   const uint8_t* chunks;
   void* Y;
   uint32_t* err;
-  uint32_t* counters;       // [tiles]
-  float* partials;          // [grid][2][64 tok][128 rows]
+  uint32_t* counters;       // [tiles]: epilogue warps of other CTAs that posted a partial of the tile
+  float* partials;          // [grid][16 token quads][128 rows][4]: at most one partial per CTA
   int64_t TR, TC, N;
   int tiles, M, out_f32, grid;
   int64_t units;            // tiles * TC
@@ -83,7 +128,6 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -97,16 +141,38 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   d |= static_cast<uint64_t>(2) << 61;                 // swizzle 128B
   return d;
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+// One k-step on one elected lane of a converged warp: D[tmem] (+)= A[tmem] *
+// B[smem]^T as 16 MMAs of M = 128, N = 64, K = 16 (MMA u = 4q + kk reads A
+// columns a + 32q + 8kk and the X box q at byte 32kk), then a commit to `bar`.
+// `accumulate` = 0 starts the accumulator afresh.  One asm block keeps the
+// issue sequence short: every extra instruction in the issuing thread
+// competes with the dequant warps for the same issue slots.
+__device__ __forceinline__ void mma_kstep(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate,
+                                          uint64_t* bar) {
+  static_assert(kXBox == 8192, "X box offsets below");
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b32 ra;\n\t.reg .b64 rb;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\tsetp.eq.b32 t, 1, 1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %5, p;\n\t"
+#define Q4NX_MMA_U(AO, BO)                                 \
+  "add.u32 ra, %1, " #AO ";\n\tadd.u64 rb, %2, " #BO ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %5, t;\n\t"
+      Q4NX_MMA_U(8, 2) Q4NX_MMA_U(16, 4) Q4NX_MMA_U(24, 6)
+      Q4NX_MMA_U(32, 512) Q4NX_MMA_U(40, 514) Q4NX_MMA_U(48, 516) Q4NX_MMA_U(56, 518)
+      Q4NX_MMA_U(64, 1024) Q4NX_MMA_U(72, 1026) Q4NX_MMA_U(80, 1028) Q4NX_MMA_U(88, 1030)
+      Q4NX_MMA_U(96, 1536) Q4NX_MMA_U(104, 1538) Q4NX_MMA_U(112, 1540) Q4NX_MMA_U(120, 1542)
+#undef Q4NX_MMA_U
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(accumulate), "r"(smem_u32(bar)), "n"(kIdesc)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+// Commit (arrive on `bar` when every MMA issued so far has completed), one elected lane.
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -122,29 +188,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+// 32 consecutive TMEM columns of this thread's lane <- r[0..31]; complete on return.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void named_bar(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// bf16x2 a + b and a * b + c, each rounded once to nearest even
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 struct Shared {
   uint64_t w_full[kWStages], w_empty[kWStages];
-  uint64_t x_full[kXStages], x_empty[kXStages];
-  uint64_t a_full[kAStages], a_empty[kAStages];
+  uint64_t full[kStages], empty[kStages];   // X (TMA bytes) + A (16 dequant warps) of a k-step
   uint64_t acc_full[kAccs], acc_empty[kAccs];
   uint64_t drain;
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
-  uint32_t last_flag;
+  uint32_t fix_seen;        // finisher's epilogue warps that have gathered every posted partial
 };
-static_assert(sizeof(Shared) <= 256, "barrier block");
+static_assert(sizeof(Shared) <= 512, "barrier block");
 
 // Bounded wait that also gives up at once when another warp has aborted.
 __device__ __forceinline__ bool wait_bar(Shared* sh, uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -161,6 +243,31 @@ __device__ __forceinline__ bool wait_bar(Shared* sh, uint64_t* bar, uint32_t par
   }
 }
 
+// wait_bar for a whole warp: true only if every lane's wait succeeded.
+__device__ __forceinline__ bool wait_bar_warp(Shared* sh, uint64_t* bar, uint32_t parity, uint32_t* err) {
+  return __all_sync(0xFFFFFFFFu, wait_bar(sh, bar, parity, err));
+}
+
+// Bounded wait (lane 0 polls, the warp follows) until `expect` partials of a
+// tile have been posted; true when they have.
+__device__ __forceinline__ bool wait_posted(Shared* sh, const uint32_t* counter, uint32_t expect, uint32_t* err,
+                                            int lane) {
+  uint32_t ok = 1u;
+  if (lane == 0 && ld_acquire_u32(counter) != expect) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_u32(counter) != expect) {
+      if (sh->abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1u;
+        atomicOr(err, 1u);
+        ok = 0u;
+        break;
+      }
+    }
+  }
+  __syncwarp();                                     // orders the other lanes' loads after lane 0's acquire
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0u;
+}
+
 // One 32-token slice of an output row: Y[m][n] for m in [m0, m0 + 32), m < M.
 __device__ __forceinline__ void store_slice(const Args& a, int64_t n, int m0, const float (&v)[32]) {
 #pragma unroll
@@ -173,43 +280,35 @@ __device__ __forceinline__ void store_slice(const Args& a, int64_t n, int m0, co
   }
 }
 
-// Decode columns [64 qq, 64 qq + 64) of weight row r of one tile row (its
-// 128-byte-swizzled code region and its scale/zero region) into row rowA of
-// an A stage (128 x 64 bf16, K-major, 128-byte swizzle).
-__device__ __forceinline__ void dequant_quarter(uint32_t codes, uint32_t scales, int r, int qq, uint32_t abase,
-                                                int rowA) {
-  // scales and zeros of groups 2qq, 2qq+1: one bf16 pair each
-  const uint32_t sw = lds_u32(scales + r * 16 + qq * 4);
-  const uint32_t zw = lds_u32(scales + 512 + r * 16 + qq * 4);
+// Columns [64 qq, 64 qq + 64) of weight row r of one tile row, as 32 bf16x2
+// words in k order: w = code*scale + zero, rounded once to bf16 (the product
+// code*scale is exact; the fused add rounds once).  The code region is
+// 128-byte swizzled (16-byte unit u of row r at u ^ (r & 7)).
+__device__ __forceinline__ void dequant_quarter(uint32_t codes, uint32_t scales, int r, int qq, uint32_t (&out)[32]) {
+  const uint32_t sw = lds_u32(scales + r * 16 + qq * 4);          // scales of groups 2qq, 2qq+1
+  const uint32_t zw = lds_u32(scales + 512 + r * 16 + qq * 4);    // zeros of the same groups
+  const uint4 c0 = lds128(codes + r * 128 + (((2 * qq) ^ (r & 7)) << 4));
+  const uint4 c1 = lds128(codes + r * 128 + (((2 * qq + 1) ^ (r & 7)) << 4));
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t kMagic = 0x43004300u;        // bf16x2 (128, 128): 128 + c is exact for c < 128
+  const uint32_t kMinus128 = 0xC300C300u;     // bf16x2 (-128, -128)
 #pragma unroll
   for (int gg = 0; gg < 2; ++gg) {
-    const int g = 2 * qq + gg;
-    const float s = __uint_as_float(gg ? (sw & 0xFFFF0000u) : (sw << 16));
-    const float z = __uint_as_float(gg ? (zw & 0xFFFF0000u) : (zw << 16));
-    // w = (1 + c 2^-8)(256 s) + (z - 256 s) for even k, (1 + c 2^-4)(16 s) + (z - 16 s) for odd k
-    const float2 s2 = make_float2(s * 256.f, s * 16.f);
-    const float2 z2 = make_float2(z - s2.x, z - s2.y);
-    const uint4 cw = lds128(codes + r * 128 + ((g ^ (r & 7)) << 4));
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    const uint32_t ONE = 0x3F800000u;
+    const uint32_t s2 = prmt(sw, 0, gg ? 0x3232u : 0x1010u);      // (s, s) of group 2qq + gg
+    const uint32_t z2 = prmt(zw, 0, gg ? 0x3232u : 0x1010u);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t w = words[t];
-      const uint32_t a15 = w << 15, a7 = w << 7, b1 = w >> 1, b9 = w >> 9;
-      const float2 v0 = make_float2(__uint_as_float(lop3_and_or(a15, 0x00078000u, ONE)),
-                                    __uint_as_float(lop3_and_or(a15, 0x00780000u, ONE)));
-      const float2 v1 = make_float2(__uint_as_float(lop3_and_or(a7, 0x00078000u, ONE)),
-                                    __uint_as_float(lop3_and_or(a7, 0x00780000u, ONE)));
-      const float2 v2 = make_float2(__uint_as_float(lop3_and_or(b1, 0x00078000u, ONE)),
-                                    __uint_as_float(lop3_and_or(b1, 0x00780000u, ONE)));
-      const float2 v3 = make_float2(__uint_as_float(lop3_and_or(b9, 0x00078000u, ONE)),
-                                    __uint_as_float(lop3_and_or(b9, 0x00780000u, ONE)));
-      const float2 w0 = ffma2(v0, s2, z2), w1 = ffma2(v1, s2, z2);
-      const float2 w2 = ffma2(v2, s2, z2), w3 = ffma2(v3, s2, z2);
-      // k within the stage = 32 gg + 8 t: 16-byte unit (4 gg + t) of the 128-byte row
-      const int unit = 4 * gg + t;
-      sts128(abase + rowA * 128 + ((unit ^ (rowA & 7)) << 4), pack_bf16x2(w0.x, w0.y), pack_bf16x2(w1.x, w1.y),
-             pack_bf16x2(w2.x, w2.y), pack_bf16x2(w3.x, w3.y));
+      const uint32_t w = words[4 * gg + t];
+      const uint32_t hi = w >> 4;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        // byte b of w holds codes k = 2b (low nibble) and 2b + 1 (high nibble):
+        // move them to bits 0-3 and 16-19, into the mantissas of 128 + c
+        const uint32_t sel = static_cast<uint32_t>(b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12));
+        const uint32_t pair = lop3_and_or(prmt(w, hi, sel), 0x000F000Fu, kMagic);
+        const uint32_t c = add_bf16x2(pair, kMinus128);                // (c_2b, c_2b+1), exact
+        out[16 * gg + 4 * t + b] = fma_bf16x2(c, s2, z2);
+      }
     }
   }
 }
@@ -226,19 +325,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t KS = a.TC;
   const int64_t first_tile = lo / KS, last_tile = (hi - 1) / KS;
   const int ntiles = static_cast<int>(last_tile - first_tile + 1);
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantWarps); }
-    for (int s = 0; s < kXStages; ++s) { mbar_init(&sh->x_full[s], 1); mbar_init(&sh->x_empty[s], 1); }
-    for (int s = 0; s < kAStages; ++s) { mbar_init(&sh->a_full[s], 4); mbar_init(&sh->a_empty[s], 1); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(&sh->full[s], 1 + kDequantWarps); mbar_init(&sh->empty[s], 1); }
     for (int s = 0; s < kAccs; ++s) { mbar_init(&sh->acc_full[s], 1); mbar_init(&sh->acc_empty[s], 4); }
     mbar_init(&sh->drain, 1);
     sh->abort_flag = 0u;
+    sh->fix_seen = 0u;
     fence_barrier_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpAlloc) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh->tmem_base)),
-                 "r"(kAccs * kTileN)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -272,154 +372,167 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpX) {
     // ----------------------------------------------------------- X
     if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");   // X may be the previous grid's output
       int64_t ks = lo % KS;
       int j = 0;
       for (; j < n; ++j) {
-        const int s = j % kXStages;
-        if (!wait_bar(sh, &sh->x_empty[s], ((j / kXStages) & 1) ^ 1u, a.err)) break;
+        const int s = j % kStages;
+        if (!wait_bar(sh, &sh->empty[s], ((j / kStages) & 1) ^ 1u, a.err)) break;
         uint8_t* st = smem + kXOff + s * kXBytes;
-        mbar_arrive_expect_tx(&sh->x_full[s], kXBytes);
+        mbar_arrive_expect_tx(&sh->full[s], kXBytes);
         for (int b = 0; b < 4; ++b)
-          tma_2d(st + b * kXBox, &xmap, static_cast<int>(ks * kStepK + b * 64), 0, &sh->x_full[s]);
+          tma_2d(st + b * kXBox, &xmap, static_cast<int>(ks * kStepK + b * 64), 0, &sh->full[s]);
         if (++ks == KS) ks = 0;
       }
-      for (int t = (j > kXStages ? j - kXStages : 0); t < j; ++t)
-        mbar_wait_bounded(&sh->x_full[t % kXStages], (t / kXStages) & 1, 100000000ull);
+      // copies still in flight land first (a stage whose dequant part stopped short stays incomplete:
+      // then the wait gives up after its limit, which only happens on the error path)
+      for (int t = (j > kStages ? j - kStages : 0); t < j; ++t)
+        mbar_wait_bounded(&sh->full[t % kStages], (t / kStages) & 1, 100000000ull);
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int64_t ks = lo % KS;
-      int tcount = 0;
-      bool first_in_tile = true;
-      for (int j = 0; j < n; ++j) {
-        const int b = tcount % kAccs;
-        if (first_in_tile) {
-          if (!wait_bar(sh, &sh->acc_empty[b], ((tcount / kAccs) & 1) ^ 1u, a.err)) break;
-          tc_fence_after();
-        }
-        const int xs = j % kXStages;
-        if (!wait_bar(sh, &sh->x_full[xs], (j / kXStages) & 1, a.err)) break;
-        const uint32_t xbase = smem_u32(smem + kXOff + xs * kXBytes);
-        bool ok = true;
-        for (int q = 0; q < kAStages; ++q) {
-          if (!wait_bar(sh, &sh->a_full[q], j & 1, a.err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t abase = smem_u32(smem + kAOff + q * kABytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = sw128_desc(abase + kk * 32);
-            const uint64_t bd = sw128_desc(xbase + q * kXBox + kk * 32);
-            mma_bf16(tmem + b * kTileN, ad, bd, (first_in_tile && q == 0 && kk == 0) ? 0u : 1u);
-          }
-          mma_commit(&sh->a_empty[q]);
-        }
-        if (!ok) break;
-        mma_commit(&sh->x_empty[xs]);
-        first_in_tile = false;
-        if (++ks == KS || j == n - 1) {             // this CTA's share of the tile is complete
-          mma_commit(&sh->acc_full[b]);
-          ++tcount;
-          first_in_tile = true;
-          if (ks == KS) ks = 0;
-        }
+    // stage s's descriptor is stage 0's plus s * kXBytes in the address field (bits 0-13, in 16-byte units)
+    const uint64_t xdesc0 = sw128_desc(smem_u32(smem + kXOff));
+    int64_t ks = lo % KS;
+    int tcount = 0;
+    bool first_in_tile = true;
+    int st = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < n; ++j) {
+      const int b = tcount & 1;
+      if (first_in_tile) {
+        if (!wait_bar_warp(sh, &sh->acc_empty[b], ((tcount >> 1) & 1) ^ 1u, a.err)) break;
       }
-      mma_commit(&sh->drain);                       // every MMA issued so far has completed
-      mbar_wait_bounded(&sh->drain, 0, 100000000ull);
+      if (!wait_bar_warp(sh, &sh->full[st], ph, a.err)) break;
+      tc_fence_after();
+      mma_kstep(tmem + static_cast<uint32_t>(b * kTileN), tmem + kTmemA + static_cast<uint32_t>(st) * kAStageCols,
+                xdesc0 + static_cast<uint64_t>(st * (kXBytes >> 4)), first_in_tile ? 0u : 1u, &sh->empty[st]);
+      first_in_tile = false;
+      if (++st == kStages) { st = 0; ph ^= 1u; }
+      if (++ks == KS || j == n - 1) {               // this CTA's share of the tile is complete
+        mma_commit_elect(&sh->acc_full[b]);
+        ++tcount;
+        first_in_tile = true;
+        if (ks == KS) ks = 0;
+      }
     }
-  } else if (warp < kWarpEpi0) {
+    mma_commit_elect(&sh->drain);                   // every MMA issued so far has completed
+    mbar_wait_bounded(&sh->drain, 0, 100000000ull);
+  } else if (warp >= kWarpDequant0 && warp < kWarpEpi0) {
     // ----------------------------------------------------------- dequant
     const int d = warp - kWarpDequant0;
-    const int i = d & 3, qq = d >> 2;
-    const int rowA = 32 * i + lane;
-    const uint32_t abase = smem_u32(smem + kAOff + qq * kABytes);
-    int64_t tile = lo / KS, ks = lo - tile * KS;
+    const int i = warp & 3, qq0 = (d >> 2) * kQuartersPerWarp;  // tile row (= TMEM lane quarter), first quarter
+    const uint32_t t_lane = static_cast<uint32_t>(32 * i) << 16;
+    int st = 0;
+    uint32_t ph = 0;
     for (int j = 0; j < n; ++j) {
       const int s = j % kWStages;
       if (!wait_bar(sh, &sh->w_full[s], (j / kWStages) & 1, a.err)) break;
-      if (!wait_bar(sh, &sh->a_empty[qq], (j & 1) ^ 1u, a.err)) break;
-      if (tile * 4 + i < a.TR) {
-        const uint32_t st = smem_u32(smem + kWOff + s * kWBytes);
-        dequant_quarter(st + i * kCodes, st + 4 * kCodes + i * kScales, lane, qq, abase, rowA);
-      }
-      fence_proxy_async_smem();
+      const uint32_t wst = smem_u32(smem + kWOff + s * kWBytes);
+      uint32_t out[kQuartersPerWarp][32];
+      // (the last tile may hold fewer than 4 tile rows: the rows past the end
+      // decode whatever the stage holds, and their results are never stored)
+#pragma unroll
+      for (int k = 0; k < kQuartersPerWarp; ++k)
+        dequant_quarter(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qq0 + k, out[k]);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sh->a_full[qq]);
-        mbar_arrive(&sh->w_empty[s]);
-      }
-      if (++ks == KS) { ks = 0; ++tile; }
+      if (lane == 0) mbar_arrive(&sh->w_empty[s]);  // the stage's bytes are in registers
+      if (!wait_bar(sh, &sh->empty[st], ph ^ 1u, a.err)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kQuartersPerWarp; ++k)
+        tmem_st32(tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols + static_cast<uint32_t>((qq0 + k) * 32),
+                  out[k]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->full[st]);
+      if (++st == kStages) { st = 0; ph ^= 1u; }
     }
-  } else {
+  } else if (warp >= kWarpEpi0) {
     // ----------------------------------------------------------- epilogue
+    asm volatile("griddepcontrol.wait;" ::: "memory");     // Y and the workspace may be the previous grid's
     const int e = warp & 3;                         // TMEM lane quarter of this warp
     const int row = 32 * e + lane;                  // row within the 128-row tile
     for (int t = 0; t < ntiles; ++t) {
-      const int b = t % kAccs;
-      if (!wait_bar(sh, &sh->acc_full[b], (t / kAccs) & 1, a.err)) break;
-      tc_fence_after();
+      const int b = t & 1;
       const int64_t tile = first_tile + t;
       const int64_t u_lo = tile * KS, u_hi = u_lo + KS;
+      const bool whole = lo <= u_lo && u_hi <= hi;   // the whole tile is computed here
+      const bool contrib = u_lo < lo;                // another CTA holds the tile's first k-step
+      const bool finisher = !whole && !contrib;
+      // finisher: the later CTAs' partials of this thread's row, summed in CTA
+      // order, gathered before the accumulator is ready (token quad k in fx[k])
+      float4 fx[kTileN / 4];
+      if (finisher) {
+        // each posting CTA counts once per epilogue warp
+        const int64_t c_last = (u_hi * a.grid - 1) / a.units;
+        if (!wait_posted(sh, &a.counters[tile], static_cast<uint32_t>(4 * (c_last - blockIdx.x)), a.err, lane))
+          break;
+        const float4* p = reinterpret_cast<const float4*>(a.partials + (blockIdx.x + 1) * (kTileN * kTileM)) + row;
+#pragma unroll
+        for (int k = 0; k < kTileN / 4; ++k) fx[k] = ld_cg_f32x4(p + k * kTileM);   // one round trip
+        for (int64_t c = blockIdx.x + 2; c <= c_last; ++c) {
+          p = reinterpret_cast<const float4*>(a.partials + c * (kTileN * kTileM)) + row;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float4 v[kTileN / 8];
+#pragma unroll
+            for (int k = 0; k < kTileN / 8; ++k) v[k] = ld_cg_f32x4(p + (8 * h + k) * kTileM);
+#pragma unroll
+            for (int k = 0; k < kTileN / 8; ++k) {
+              float4& f = fx[8 * h + k];
+              f = make_float4(f.x + v[k].x, f.y + v[k].y, f.z + v[k].z, f.w + v[k].w);
+            }
+          }
+        }
+        // the last epilogue warp through clears the count for the next launch
+        if (lane == 0 && atomicAdd(&sh->fix_seen, 1u) == 3u) a.counters[tile] = 0u;
+      }
+      if (!wait_bar(sh, &sh->acc_full[b], (t >> 1) & 1, a.err)) break;
+      tc_fence_after();
       const int64_t n0 = tile * kTileM;
       const bool valid_row = n0 + row < a.N;
-      const bool whole = lo <= u_lo && u_hi <= hi;   // the whole tile was computed here
-      const int slot = (lo >= u_lo) ? 0 : 1;          // split tile: this CTA's partial slot
-      float* mine = a.partials + (static_cast<int64_t>(blockIdx.x) * 2 + slot) * (kTileN * kTileM) + row;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + b * kTileN;
-#pragma unroll 1
+      float4* mine = reinterpret_cast<float4*>(a.partials + static_cast<int64_t>(blockIdx.x) * (kTileN * kTileM)) + row;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + static_cast<uint32_t>(b * kTileN);
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v[32];
         tmem_ld32(taddr + 32 * h, v);
-        if (whole) {
-          if (valid_row) store_slice(a, n0 + row, 32 * h, v);
-        } else {
+        if (contrib) {
 #pragma unroll
-          for (int m = 0; m < 32; ++m) mine[(32 * h + m) * kTileM] = v[m];
+          for (int k = 0; k < 8; ++k)
+            mine[(8 * h + k) * kTileM] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        } else {
+          if (finisher) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] += fx[8 * h + k].x;
+              v[4 * k + 1] += fx[8 * h + k].y;
+              v[4 * k + 2] += fx[8 * h + k].z;
+              v[4 * k + 3] += fx[8 * h + k].w;
+            }
+          }
+          if (valid_row) store_slice(a, n0 + row, 32 * h, v);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
-      if (whole) continue;
-      // split tile: the last CTA to arrive adds the partials (in CTA order) and stores the tile
-      __threadfence();
-      named_bar(1, 128);
-      const int64_t c_first = ((u_lo + 1) * a.grid - 1) / a.units;
-      const int64_t c_last = (u_hi * a.grid - 1) / a.units;
-      if (threadIdx.x == kWarpEpi0 * 32) {
-        const uint32_t old = atomicAdd(&a.counters[tile], 1u);
-        sh->last_flag = (old == static_cast<uint32_t>(c_last - c_first)) ? 1u : 0u;
+      if (contrib) {
+        // post this warp's rows of the partial: every lane's stores, then one release count
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_add(&a.counters[tile], 1u);
       }
-      named_bar(1, 128);
-      const bool last = sh->last_flag != 0u;
-      named_bar(1, 128);                            // every thread has read the flag before it is reused
-      if (!last) continue;
-      __threadfence();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float v[32];
-#pragma unroll
-        for (int m = 0; m < 32; ++m) v[m] = 0.f;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-          const int64_t clo = a.units * c / a.grid;
-          float* p = a.partials + (c * 2 + ((clo >= u_lo) ? 0 : 1)) * (kTileN * kTileM) + row + 32 * h * kTileM;
-#pragma unroll
-          for (int m = 0; m < 32; ++m) v[m] += ld_cg_f32(p + m * kTileM);
-#pragma unroll
-          for (int m = 0; m < 32; ++m) p[m * kTileM] = 0.f;    // leave the workspace zero-filled
-        }
-        if (valid_row) store_slice(a, n0 + row, 32 * h, v);
-      }
-      if (threadIdx.x == kWarpEpi0 * 32) a.counters[tile] = 0u;
     }
   }
 
   __syncwarp();                                     // whole warps arrive at the CTA barrier
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpAlloc) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kAccs * kTileN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -451,9 +564,9 @@ uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M) {
   (void)TC;
   (void)M;
   const int64_t tiles = (TR + 3) / 4;
-  // error word, arrival counters, partial tiles of at most 1024 CTAs
+  // error word, posting counters, one partial tile per CTA (at most 1024 CTAs)
   return kWsErrBytes + align16(static_cast<uint64_t>(tiles) * 4) +
-         static_cast<uint64_t>(1024) * 2 * gemm::kTileN * gemm::kTileM * 4;
+         static_cast<uint64_t>(1024) * gemm::kTileN * gemm::kTileM * 4;
 }
 
 cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, const void* X, int M, void* Y,
@@ -503,12 +616,26 @@ cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, co
   a.M = M;
   a.out_f32 = out_f32;
   a.units = tiles * TC;
-  int64_t grid = info.sms < 1024 ? info.sms : 1024;
-  if (grid > a.units) grid = a.units;
+  // at least 4 k-steps per CTA where the work allows it, at most one CTA per SM
+  int64_t grid = (a.units + 3) / 4;
+  if (grid > info.sms) grid = info.sms;
+  if (grid > 1024) grid = 1024;
+  if (grid < 1) grid = 1;
   a.grid = static_cast<int>(grid);
   e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm::gemm_q41_kernel), 16);
   if (e != cudaSuccess) return e;
-  gemm::gemm_q41_kernel<<<a.grid, gemm::kThreads, gemm::kSmemBytes, s>>>(wmap, xmap, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid);
+  cfg.blockDim = dim3(gemm::kThreads);
+  cfg.dynamicSmemBytes = gemm::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_q41_kernel, wmap, xmap, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -98,14 +98,6 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
   else static_cast<uint16_t*>(y)[n] = f32_to_bf16_bits(v);
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // A tile row [r0, r1) shared with other CTAs, after this CTA's warps have
 // combined their parts (lane = row, `val` = this CTA's sum).  The CTA holding
