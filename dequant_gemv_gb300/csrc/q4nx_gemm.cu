@@ -19,20 +19,25 @@
 // alone, and the TMA fills, the code reads and the B reads need that bandwidth.
 //
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31 only):
-//   warp 0       weight producer: per k-step the 4 chunks' code regions (3-D
-//                tensor copy, 128-byte swizzle, so that row-wise 16-byte reads
-//                are free of bank conflicts) and scale/zero regions (1-D bulk
-//                copies) into one of kWStages stages;
-//   warp 1       X producer: the 64 x 256 bf16 slice of X (4 boxes of 64 x 64)
-//                into one of kStages stages;
+//   warp 0       weight producer: per k-step the 4 chunks' code regions (one
+//                4-D tensor copy, 128-byte swizzle, so that row-wise 16-byte
+//                reads are free of bank conflicts) and their scale/zero regions
+//                (one 4-D tensor copy) into one of kWStages stages;
+//   warp 1       X producer: the 64 x 256 bf16 slice of X (one 3-D tensor copy
+//                of 4 boxes of 64 x 64) into one of kStages stages;
+// The producers, like the MMA warp, run their loops warp-wide and issue from
+// one elected lane: a copy instruction issued from a single-lane branch costs
+// far more issue slots, and these slots are shared with the dequant warps.
 //   warp 2       MMA issuer: the whole warp runs the loop (its values stay
 //                warp-uniform) and one elected lane issues each k-step's 16
 //                MMAs and their commit as one block;
 //   warp 3       TMEM allocator;
 //   warps 4-11   dequant: warp w decodes tile row w%4 (the TMEM lanes of that
-//                tile row), columns 128*((w-4)/4) .. +127 of the k-step, one
-//                thread per weight row, into the A half of one of kStages
-//                stages (the A half in TMEM, the X half in shared memory);
+//                tile row) for the k-steps of parity (w-4)/4, one thread per
+//                weight row, into the A half of one of kStages stages (the A
+//                half in TMEM, the X half in shared memory).  The two warps of
+//                a tile row take alternate k-steps, so each pays its per-step
+//                barrier traffic once per whole k-step of work;
 //   warps 12-15  epilogue: TMEM -> registers -> Y, or a split-tile partial.
 // Eight dequant warps rather than sixteen: the MMA warp shares its
 // sub-partition's issue slots with the dequant warps there, and fewer of them
@@ -53,6 +58,11 @@
 // then the finisher's own), so results are deterministic.  Every wait is
 // bounded; if one gives up, the CTA records the error in the workspace and
 // winds down.
+//
+// A CTA's last tile leaves through shared memory (the X stages are free once
+// its last MMA has completed): the epilogue warps stage the tile there and one
+// thread writes it with a single bulk copy (a TMA tensor store for Y, a 1-D
+// bulk store for a partial), instead of thousands of small scattered stores.
 //
 // The finisher waits for CTAs of the same launch, so the launch relies on all
 // of its CTAs being resident at once: the grid is at most one CTA per SM, and
@@ -80,8 +90,8 @@ constexpr int kWOff = 0;
 constexpr int kXOff = kWOff + kWStages * kWBytes;
 constexpr int kBarOff = kXOff + kStages * kXBytes;
 constexpr int kSmemBytes = kBarOff + 512 + 1024;       // barriers and flags, alignment slack
-constexpr int kDequantWarps = 8;
-constexpr int kQuartersPerWarp = 16 / kDequantWarps;   // 64-column quarters of a k-step per dequant warp
+constexpr int kDequantWarps = 8;                       // two per TMEM lane quarter, alternate k-steps
+constexpr int kDequantPerStep = 4;                     // dequant warps that fill one k-step (one per tile row)
 constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpAlloc = 3, kWarpDequant0 = 4;
 constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
 constexpr int kWarps = kWarpEpi0 + 4;
@@ -113,16 +123,29 @@ struct Args {
 
 // --------------------------------------------------------------- PTX ----
 
-__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+// One k-step of weights, on one elected lane of a converged warp: arm `bar`
+// for kWBytes, then copy the code regions of chunks (4 tr4 + i, ks), i < 4,
+// to dst + 4096 i and their scale/zero regions to dst + 16384 + 1024 i (tile
+// rows past the end read as zeros and still count their bytes).
+__device__ __forceinline__ void issue_weights(uint32_t dst, const CUtensorMap* cmap, const CUtensorMap* smap, int ks,
+                                              int tr4, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%5], %6;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%2, {0, 0, %3, %4}], [%5];\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%1], [%7, {0, 0, %3, %4}], [%5];\n\t}"
+      ::"r"(dst), "r"(dst + 4 * 4096), "l"(reinterpret_cast<uint64_t>(cmap)), "r"(ks), "r"(tr4), "r"(bar),
+      "n"(4 * 4096 + 4 * 1024), "l"(reinterpret_cast<uint64_t>(smap))
       : "memory");
 }
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+// One k-step of X, on one elected lane: arm `bar` for 32 KB, then copy
+// X[0:64, 256 ks .. +255] as 4 boxes of 64 tokens x 64 k (128-byte swizzle).
+__device__ __forceinline__ void issue_x(uint32_t dst, const CUtensorMap* xmap, int ks, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {0, 0, %2}], [%3];\n\t}"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(xmap)), "r"(4 * ks), "r"(bar), "n"(4 * 64 * 128)
       : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -188,18 +211,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 32 consecutive TMEM columns of this thread's lane <- r[0..31]; complete on return.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void sts_f32x4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+// shared -> global copies issued by one thread; `wait_written` returns once the
+// data is in global memory, `wait_read` once the shared source may be reused.
+__device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t ssrc) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(ssrc)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_written() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -219,9 +254,10 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
 
 struct Shared {
   uint64_t w_full[kWStages], w_empty[kWStages];
-  uint64_t full[kStages], empty[kStages];   // X (TMA bytes) + A (16 dequant warps) of a k-step
+  uint64_t full[kStages], empty[kStages];   // X (TMA bytes) + A (4 dequant warps) of a k-step
   uint64_t acc_full[kAccs], acc_empty[kAccs];
   uint64_t drain;
+  uint64_t staged;          // epilogue warps that have staged their rows of the last tile
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   uint32_t fix_seen;        // finisher's epilogue warps that have gathered every posted partial
@@ -233,7 +269,7 @@ __device__ __forceinline__ bool wait_bar(Shared* sh, uint64_t* bar, uint32_t par
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (sh->abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       sh->abort_flag = 1u;
@@ -280,25 +316,28 @@ __device__ __forceinline__ void store_slice(const Args& a, int64_t n, int m0, co
   }
 }
 
-// Columns [64 qq, 64 qq + 64) of weight row r of one tile row, as 32 bf16x2
-// words in k order: w = code*scale + zero, rounded once to bf16 (the product
-// code*scale is exact; the fused add rounds once).  The code region is
-// 128-byte swizzled (16-byte unit u of row r at u ^ (r & 7)).
-__device__ __forceinline__ void dequant_quarter(uint32_t codes, uint32_t scales, int r, int qq, uint32_t (&out)[32]) {
-  const uint32_t sw = lds_u32(scales + r * 16 + qq * 4);          // scales of groups 2qq, 2qq+1
-  const uint32_t zw = lds_u32(scales + 512 + r * 16 + qq * 4);    // zeros of the same groups
-  const uint4 c0 = lds128(codes + r * 128 + (((2 * qq) ^ (r & 7)) << 4));
-  const uint4 c1 = lds128(codes + r * 128 + (((2 * qq + 1) ^ (r & 7)) << 4));
-  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+// Columns [128 qh, 128 qh + 128) of weight row r of one tile row, as 64
+// bf16x2 words in k order: w = code*scale + zero, rounded once to bf16 (the
+// product code*scale is exact; the fused add rounds once).  The code region
+// is 128-byte swizzled (16-byte unit u of row r at u ^ (r & 7)).  All shared
+// memory loads come first, so their latency is paid once.
+__device__ __forceinline__ void dequant_half(uint32_t codes, uint32_t scales, int r, int qh, uint32_t (&out)[64]) {
+  const uint2 sw = lds64(scales + r * 16 + qh * 8);                // scales of groups 4qh .. 4qh+3
+  const uint2 zw = lds64(scales + 512 + r * 16 + qh * 8);          // zeros of the same groups
+  uint4 cw[4];
+#pragma unroll
+  for (int gg = 0; gg < 4; ++gg) cw[gg] = lds128(codes + r * 128 + (((4 * qh + gg) ^ (r & 7)) << 4));
   const uint32_t kMagic = 0x43004300u;        // bf16x2 (128, 128): 128 + c is exact for c < 128
   const uint32_t kMinus128 = 0xC300C300u;     // bf16x2 (-128, -128)
 #pragma unroll
-  for (int gg = 0; gg < 2; ++gg) {
-    const uint32_t s2 = prmt(sw, 0, gg ? 0x3232u : 0x1010u);      // (s, s) of group 2qq + gg
-    const uint32_t z2 = prmt(zw, 0, gg ? 0x3232u : 0x1010u);
+  for (int gg = 0; gg < 4; ++gg) {
+    const uint32_t sp = gg < 2 ? sw.x : sw.y, zp = gg < 2 ? zw.x : zw.y;
+    const uint32_t s2 = prmt(sp, 0, (gg & 1) ? 0x3232u : 0x1010u);  // (s, s) of group 4qh + gg
+    const uint32_t z2 = prmt(zp, 0, (gg & 1) ? 0x3232u : 0x1010u);
+    const uint32_t words[4] = {cw[gg].x, cw[gg].y, cw[gg].z, cw[gg].w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t w = words[4 * gg + t];
+      const uint32_t w = words[t];
       const uint32_t hi = w >> 4;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -312,9 +351,22 @@ __device__ __forceinline__ void dequant_quarter(uint32_t codes, uint32_t scales,
     }
   }
 }
+// 32 consecutive TMEM columns of this thread's lane <- r[0..31]; in flight on
+// return (tcgen05.wait::st completes it).
+__device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q41_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+    gemm_q41_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+                    const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
                     const __grid_constant__ Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,10 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantWarps); }
-    for (int s = 0; s < kStages; ++s) { mbar_init(&sh->full[s], 1 + kDequantWarps); mbar_init(&sh->empty[s], 1); }
+    for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantPerStep); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(&sh->full[s], 1 + kDequantPerStep); mbar_init(&sh->empty[s], 1); }
     for (int s = 0; s < kAccs; ++s) { mbar_init(&sh->acc_full[s], 1); mbar_init(&sh->acc_empty[s], 4); }
     mbar_init(&sh->drain, 1);
+    mbar_init(&sh->staged, 4);
     sh->abort_flag = 0u;
     sh->fix_seen = 0u;
     fence_barrier_init();
@@ -349,46 +402,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpW) {
     // ----------------------------------------------------------- weights
-    if (lane == 0) {
-      int64_t tile = lo / KS, ks = lo - tile * KS;
-      int j = 0;
-      for (; j < n; ++j) {
-        const int s = j % kWStages;
-        if (!wait_bar(sh, &sh->w_empty[s], ((j / kWStages) & 1) ^ 1u, a.err)) break;
-        uint8_t* st = smem + kWOff + s * kWBytes;
-        const int64_t left = a.TR - tile * 4;
-        const int rows = left < 4 ? static_cast<int>(left) : 4;
-        mbar_arrive_expect_tx(&sh->w_full[s], rows * (kCodes + kScales));
-        for (int i = 0; i < rows; ++i) {
-          const int64_t chunk = (tile * 4 + i) * a.TC + ks;
-          tma_3d(st + i * kCodes, &wmap, 0, 0, static_cast<int>(chunk), &sh->w_full[s]);
-          bulk_g2s(st + 4 * kCodes + i * kScales, a.chunks + chunk * kQ41Bytes + kQ41Scale, kScales, &sh->w_full[s]);
-        }
-        if (++ks == KS) { ks = 0; ++tile; }
-      }
-      for (int t = (j > kWStages ? j - kWStages : 0); t < j; ++t)      // copies still in flight land first
-        mbar_wait_bounded(&sh->w_full[t % kWStages], (t / kWStages) & 1, 100000000ull);
+    int64_t tile = lo / KS, ks = lo - tile * KS;
+    int j = 0;
+    for (; j < n; ++j) {
+      const int s = j % kWStages;
+      if (!wait_bar_warp(sh, &sh->w_empty[s], ((j / kWStages) & 1) ^ 1u, a.err)) break;
+      issue_weights(smem_u32(smem + kWOff + s * kWBytes), &wmap, &smap, static_cast<int>(ks), static_cast<int>(tile * 4),
+                    smem_u32(&sh->w_full[s]));
+      if (++ks == KS) { ks = 0; ++tile; }
     }
+    for (int t = (j > kWStages ? j - kWStages : 0); t < j; ++t)        // copies still in flight land first
+      mbar_wait_bounded(&sh->w_full[t % kWStages], (t / kWStages) & 1, 100000000ull);
   } else if (warp == kWarpX) {
     // ----------------------------------------------------------- X
-    if (lane == 0) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");   // X may be the previous grid's output
-      int64_t ks = lo % KS;
-      int j = 0;
-      for (; j < n; ++j) {
-        const int s = j % kStages;
-        if (!wait_bar(sh, &sh->empty[s], ((j / kStages) & 1) ^ 1u, a.err)) break;
-        uint8_t* st = smem + kXOff + s * kXBytes;
-        mbar_arrive_expect_tx(&sh->full[s], kXBytes);
-        for (int b = 0; b < 4; ++b)
-          tma_2d(st + b * kXBox, &xmap, static_cast<int>(ks * kStepK + b * 64), 0, &sh->full[s]);
-        if (++ks == KS) ks = 0;
-      }
-      // copies still in flight land first (a stage whose dequant part stopped short stays incomplete:
-      // then the wait gives up after its limit, which only happens on the error path)
-      for (int t = (j > kStages ? j - kStages : 0); t < j; ++t)
-        mbar_wait_bounded(&sh->full[t % kStages], (t / kStages) & 1, 100000000ull);
+    asm volatile("griddepcontrol.wait;" ::: "memory");     // X may be the previous grid's output
+    int64_t ks = lo % KS;
+    int j = 0;
+    for (; j < n; ++j) {
+      const int s = j % kStages;
+      if (!wait_bar_warp(sh, &sh->empty[s], ((j / kStages) & 1) ^ 1u, a.err)) break;
+      issue_x(smem_u32(smem + kXOff + s * kXBytes), &xmap, static_cast<int>(ks), smem_u32(&sh->full[s]));
+      if (++ks == KS) ks = 0;
     }
+    // copies still in flight land first (a stage whose dequant part stopped short stays incomplete:
+    // then the wait gives up after its limit, which only happens on the error path)
+    for (int t = (j > kStages ? j - kStages : 0); t < j; ++t)
+      mbar_wait_bounded(&sh->full[t % kStages], (t / kStages) & 1, 100000000ull);
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------- MMA issuer
     // stage s's descriptor is stage 0's plus s * kXBytes in the address field (bits 0-13, in 16-byte units)
@@ -420,33 +459,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(&sh->drain, 0, 100000000ull);
   } else if (warp >= kWarpDequant0 && warp < kWarpEpi0) {
     // ----------------------------------------------------------- dequant
-    const int d = warp - kWarpDequant0;
-    const int i = warp & 3, qq0 = (d >> 2) * kQuartersPerWarp;  // tile row (= TMEM lane quarter), first quarter
+    // Software-pipelined: the TMEM stores of a k-step stay in flight while the
+    // warp decodes its next k-step; only then are they completed and
+    // announced.  The barriers a step needs are tested (without blocking) one
+    // step ahead, so the round trip of the test overlaps the decode; a step
+    // blocks only if its stage is really not ready.
+    const int i = warp & 3, par = (warp - kWarpDequant0) >> 2;  // tile row (= TMEM lane quarter), k-step parity
     const uint32_t t_lane = static_cast<uint32_t>(32 * i) << 16;
-    int st = 0;
-    uint32_t ph = 0;
-    for (int j = 0; j < n; ++j) {
-      const int s = j % kWStages;
-      if (!wait_bar(sh, &sh->w_full[s], (j / kWStages) & 1, a.err)) break;
-      const uint32_t wst = smem_u32(smem + kWOff + s * kWBytes);
-      uint32_t out[kQuartersPerWarp][32];
+    int pst = -1;                                   // stage stored but not yet announced
+    // this warp's k-steps j = par, par + 2, ...: A/X stage j % kStages with phase (j / kStages) & 1,
+    // weight stage j % kWStages with phase (j / kWStages) & 1
+    bool w_ok = par < n ? mbar_test_wait(&sh->w_full[par % kWStages], (par / kWStages) & 1) : true;
+    for (int j = par; j < n; j += 2) {
+      const int ws = j % kWStages, st = j % kStages;
+      const uint32_t wph = (j / kWStages) & 1, ph = (j / kStages) & 1;
+      if (!__all_sync(0xFFFFFFFFu, w_ok) && !wait_bar_warp(sh, &sh->w_full[ws], wph, a.err)) break;
+      const int jn = j + 2;
+      const bool w_ok_next = jn < n ? mbar_test_wait(&sh->w_full[jn % kWStages], (jn / kWStages) & 1) : true;
+      const bool e_ok = mbar_test_wait(&sh->empty[st], ph ^ 1u);
+      const uint32_t wst = smem_u32(smem + kWOff + ws * kWBytes);
+      const uint32_t tdst = tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols;
       // (the last tile may hold fewer than 4 tile rows: the rows past the end
       // decode whatever the stage holds, and their results are never stored)
-#pragma unroll
-      for (int k = 0; k < kQuartersPerWarp; ++k)
-        dequant_quarter(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qq0 + k, out[k]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->w_empty[s]);  // the stage's bytes are in registers
-      if (!wait_bar(sh, &sh->empty[st], ph ^ 1u, a.err)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < kQuartersPerWarp; ++k)
-        tmem_st32(tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols + static_cast<uint32_t>((qq0 + k) * 32),
-                  out[k]);
+#pragma unroll 1
+      for (int qh = 0; qh < 2; ++qh) {
+        uint32_t out[64];
+        dequant_half(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qh, out);
+        if (qh == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->w_empty[ws]);   // the stage's bytes are in registers
+        }
+        if (pst >= 0) {                             // the previous k-step's stores, completed and announced
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->full[pst]);
+          pst = -1;
+        }
+        if (qh == 0 && !__all_sync(0xFFFFFFFFu, e_ok) && !wait_bar_warp(sh, &sh->empty[st], ph ^ 1u, a.err)) {
+          pst = -2;                                 // give up (error path)
+          break;
+        }
+        tc_fence_after();
+        tmem_st32_async(tdst + static_cast<uint32_t>(qh * 64), out);
+        tmem_st32_async(tdst + static_cast<uint32_t>(qh * 64 + 32), out + 32);
+      }
+      if (pst == -2) break;
+      pst = st;
+      w_ok = w_ok_next;
+    }
+    if (pst >= 0) {
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->full[st]);
-      if (++st == kStages) { st = 0; ph ^= 1u; }
+      if (lane == 0) mbar_arrive(&sh->full[pst]);
     }
   } else if (warp >= kWarpEpi0) {
     // ----------------------------------------------------------- epilogue
@@ -494,6 +560,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid_row = n0 + row < a.N;
       float4* mine = reinterpret_cast<float4*>(a.partials + static_cast<int64_t>(blockIdx.x) * (kTileN * kTileM)) + row;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + static_cast<uint32_t>(b * kTileN);
+      if (t == ntiles - 1) {
+        // last tile: stage it in X stage 0 ([16 quads][128 rows][4] fp32 for a
+        // partial, [64 tokens][128 rows] of the output type for Y), then one
+        // thread writes it out with a single bulk copy
+        const uint32_t stg = smem_u32(smem + kXOff);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float v[32];
+          tmem_ld32(taddr + 32 * h, v);
+          if (contrib) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              sts_f32x4(stg + static_cast<uint32_t>(((8 * h + k) * kTileM + row) * 16), v[4 * k], v[4 * k + 1],
+                        v[4 * k + 2], v[4 * k + 3]);
+          } else {
+            if (finisher) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                v[4 * k] += fx[8 * h + k].x;
+                v[4 * k + 1] += fx[8 * h + k].y;
+                v[4 * k + 2] += fx[8 * h + k].z;
+                v[4 * k + 3] += fx[8 * h + k].w;
+              }
+            }
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+              const uint32_t idx = static_cast<uint32_t>((32 * h + m) * kTileM + row);
+              if (a.out_f32) sts_f32(stg + idx * 4, v[m]);
+              else sts_u16(stg + idx * 2, f32_to_bf16_bits(v[m]));
+            }
+          }
+        }
+        tc_fence_before();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staged bytes visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh->acc_empty[b]);
+          mbar_arrive(&sh->staged);
+        }
+        if (warp == kWarpEpi0 && lane == 0) {
+          if (!wait_bar(sh, &sh->staged, 0, a.err)) break;
+          if (contrib) {
+            bulk_s2g(a.partials + static_cast<int64_t>(blockIdx.x) * (kTileN * kTileM), stg, kTileN * kTileM * 4);
+            bulk_commit();
+            bulk_wait_written();
+            asm volatile("fence.proxy.async.global;" ::: "memory");     // the copy's writes before the count
+            red_release_add(&a.counters[tile], 4u);                     // all four epilogue warps' rows
+          } else {
+            tma_store_2d(&ymap, static_cast<int>(n0), 0, stg);
+            bulk_commit();
+            bulk_wait_read();
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float v[32];
@@ -579,25 +700,48 @@ cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, co
   if (e != cudaSuccess) return e;
   if (info.max_smem_optin < gemm::kSmemBytes) return cudaErrorNotSupported;
 
-  CUtensorMap wmap, xmap;
-  const int64_t T = TR * TC;
+  // weights: code regions as [128 B][32 rows][TC chunk columns][TR tile rows] (128-byte swizzle) and
+  // scale/zero regions as [256 B][4][TC][TR] from byte 4096 of each chunk; X as [64 k][M tokens][K / 64]
+  CUtensorMap wmap, smap, xmap, ymap;
   {
-    cuuint64_t dims[3] = {128, 32, static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[2] = {128, kQ41Bytes};
-    cuuint32_t box[3] = {128, 32, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(chunks), dims, strides, box, es,
+    cuuint64_t dims[4] = {128, 32, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
+    cuuint64_t strides[3] = {128, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
+    cuuint32_t box[4] = {128, 32, 1, 4};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(chunks), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(TC * 256), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(TC * 256 * 2)};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, es,
+    cuuint64_t dims[4] = {256, 4, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
+    cuuint64_t strides[3] = {256, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
+    cuuint32_t box[4] = {256, 4, 1, 4};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(chunks) + kQ41Scale);
+    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(TC * 4)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(TC * 256 * 2), 128};
+    cuuint32_t box[3] = {64, 64, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(X), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // Y [M][N] of the output type, box of 128 rows x 64 tokens (rows or tokens past the end are not written)
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(TR * 32), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(TR * 32) * (out_f32 ? 4u : 2u)};
+    cuuint32_t box[2] = {128, 64};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&ymap, out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Y, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -634,7 +778,7 @@ cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm::gemm_q41_kernel, wmap, xmap, a);
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_q41_kernel, wmap, smap, xmap, ymap, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
