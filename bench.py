@@ -463,16 +463,16 @@ def run_suite(args):
             alg = nb + rep.numel()
             emit({"suite": "repack", "workload": name, "us": us,
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
-        if kind == synth.Q4_1 and wid == 4 and want("gemm_m64"):
+        if ((kind == synth.Q4_1 and wid == 4) or wid == 5) and want("gemm_m64"):
             M = 64
             X = dev_bf16(synth.workload_activations(wid, 0, M, K))
-            Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            Y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
             with torch.cuda.stream(stream):
                 gws = torch.zeros(int(q.lib.q4nx_gemm_workspace(ctypes.byref(Ws[0].c()), M)), dtype=torch.uint8,
                                   device=dev)
-            us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, ws=gws) for W in Ws], 400)
+            us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, out_dtype=od, ws=gws) for W in Ws], 400)
             flops = 2.0 * M * N * K
-            alg = nb + 2 * M * K + 2 * M * N
+            alg = nb + 2 * M * K + (4 if out_f32 else 2) * M * N
             t_roof = max(alg / (hbm * 1e3), flops / (tc_peak * 1e6))
             emit({"suite": "gemm_m64", "workload": name, "M": M, "us": us, "tflops": flops / us / 1e6,
                   "weight_gbs": nb / us / 1e3,

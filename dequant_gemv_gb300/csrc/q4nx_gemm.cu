@@ -1,8 +1,9 @@
 // q4nx_gemm.cu -- fused decode + GEMM for a block of up to 64 tokens on the
 // 5th-generation tensor cores (tcgen05, TMEM, TMA), sm_103a.
 //
-//   Y[m][n] = sum_k X[m][k] * w[n][k],   w in q4_1 chunks ("Q4NX chunks"
-//   section of the 1bit engine "NPU engine" page: code*scale + zero).
+//   Y[m][n] = sum_k X[m][k] * w[n][k],   w in q4_1 chunks (code*scale + zero)
+//   or Q8 chunks in either code layout (d*code); "Q4NX chunks" section of the
+//   1bit engine "NPU engine" page.
 //
 // Tile: 128 weight rows (4 tile rows of the chunk grid) x 64 tokens; k-steps
 // of 256 columns (one chunk column).  The weight rows are the MMA's M side and
@@ -19,10 +20,12 @@
 // alone, and the TMA fills, the code reads and the B reads need that bandwidth.
 //
 // Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31 only):
-//   warp 0       weight producer: per k-step the 4 chunks' code regions (one
-//                4-D tensor copy, 128-byte swizzle, so that row-wise 16-byte
-//                reads are free of bank conflicts) and their scale/zero regions
-//                (one 4-D tensor copy) into one of kWStages stages;
+//   warp 0       weight producer: per k-step the 4 chunks into one of the
+//                weight stages.  q4_1: the code regions (one 4-D tensor copy,
+//                128-byte swizzle, so that row-wise 16-byte reads are free of
+//                bank conflicts) and the scale/zero regions (one 4-D tensor
+//                copy); Q8: the 4 whole chunks (one 4-D tensor copy), whose
+//                column-wise codes the dequant warps read a byte at a time;
 //   warp 1       X producer: the 64 x 256 bf16 slice of X (one 3-D tensor copy
 //                of 4 boxes of 64 x 64) into one of kStages stages;
 // The producers, like the MMA warp, run their loops warp-wide and issue from
@@ -33,11 +36,9 @@
 //                MMAs and their commit as one block;
 //   warp 3       TMEM allocator;
 //   warps 4-11   dequant: warp w decodes tile row w%4 (the TMEM lanes of that
-//                tile row) for the k-steps of parity (w-4)/4, one thread per
-//                weight row, into the A half of one of kStages stages (the A
-//                half in TMEM, the X half in shared memory).  The two warps of
-//                a tile row take alternate k-steps, so each pays its per-step
-//                barrier traffic once per whole k-step of work;
+//                tile row), columns 128*((w-4)/4) .. +127 of every k-step, one
+//                thread per weight row, into the A half of one of kStages
+//                stages (the A half in TMEM, the X half in shared memory);
 //   warps 12-15  epilogue: TMEM -> registers -> Y, or a split-tile partial.
 // Eight dequant warps rather than sixteen: the MMA warp shares its
 // sub-partition's issue slots with the dequant warps there, and fewer of them
@@ -81,17 +82,26 @@ namespace q4nx {
 namespace gemm {
 
 constexpr int kTileM = 128, kTileN = 64, kStepK = 256;
-constexpr int kWStages = 6, kStages = 3, kAccs = 2;
-constexpr int kCodes = 4096, kScales = 1024;
-constexpr int kWBytes = 4 * kCodes + 4 * kScales;     // 20 KB: codes (1024-aligned) then scales
+constexpr int kStages = 3, kAccs = 2;
+constexpr int kCodes = 4096, kScales = 1024;            // q4_1 stage: codes (1024-aligned), then scales and zeros
 constexpr int kXBox = 64 * 128;                        // 64 tokens x 64 k of bf16
 constexpr int kXBytes = 4 * kXBox;                     // 32 KB
 constexpr int kWOff = 0;
-constexpr int kXOff = kWOff + kWStages * kWBytes;
-constexpr int kBarOff = kXOff + kStages * kXBytes;
-constexpr int kSmemBytes = kBarOff + 512 + 1024;       // barriers and flags, alignment slack
-constexpr int kDequantWarps = 8;                       // two per TMEM lane quarter, alternate k-steps
-constexpr int kDequantPerStep = 4;                     // dequant warps that fill one k-step (one per tile row)
+constexpr int kMaxWStages = 6;
+// Shared-memory plan per chunk kind: weight stages, then X stages, then barriers.
+template <int KIND>
+struct Plan {
+  static constexpr bool kQ8 = KIND == kQ8_KR || KIND == kQ8_BLK;
+  static constexpr int kWBytes = kQ8 ? 4 * kQ8Bytes : 4 * kCodes + 4 * kScales;   // one k-step of 4 chunks
+  static constexpr int kWStages = kQ8 ? 3 : 6;
+  static constexpr int kXOff = kWOff + kWStages * kWBytes;
+  static constexpr int kBarOff = kXOff + kStages * kXBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;   // barriers and flags, alignment slack
+  static_assert(kWStages <= kMaxWStages, "weight stages");
+  static_assert(kWBytes % 1024 == 0 && kXOff % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions 1024-aligned");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+constexpr int kDequantWarps = 8;                       // two per TMEM lane quarter, one half of the k-step each
 constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpAlloc = 3, kWarpDequant0 = 4;
 constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
 constexpr int kWarps = kWarpEpi0 + 4;
@@ -104,8 +114,6 @@ constexpr uint32_t kAStageCols = kStepK / 2;
 static_assert(kTmemA + kStages * kAStageCols <= kTmemCols, "TMEM budget");
 static_assert(kWarpDequant0 % 4 == 0 && kWarpEpi0 % 4 == 0, "TMEM lane quarters follow warp % 4");
 static_assert(kDequantWarps == 8, "dequant warps: two per TMEM lane quarter");
-static_assert(kWBytes % 1024 == 0 && kXOff % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions 1024-aligned");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // tcgen05 instruction descriptor: D fp32, A bf16, B bf16, both K-major, N = 64, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kTileN >> 3) << 17) | ((kTileM >> 4) << 24);
@@ -136,6 +144,16 @@ __device__ __forceinline__ void issue_weights(uint32_t dst, const CUtensorMap* c
       "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%1], [%7, {0, 0, %3, %4}], [%5];\n\t}"
       ::"r"(dst), "r"(dst + 4 * 4096), "l"(reinterpret_cast<uint64_t>(cmap)), "r"(ks), "r"(tr4), "r"(bar),
       "n"(4 * 4096 + 4 * 1024), "l"(reinterpret_cast<uint64_t>(smap))
+      : "memory");
+}
+// Q8: one k-step of weights, on one elected lane: arm `bar` for 4 chunks,
+// then copy chunks (4 tr4 + i, ks), i < 4, whole to dst + 8704 i.
+__device__ __forceinline__ void issue_weights_q8(uint32_t dst, const CUtensorMap* map, int ks, int tr4, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%5, {0, 0, %1, %2}], [%3];\n\t}"
+      ::"r"(dst), "r"(ks), "r"(tr4), "r"(bar), "n"(4 * kQ8Bytes), "l"(reinterpret_cast<uint64_t>(map))
       : "memory");
 }
 // One k-step of X, on one elected lane: arm `bar` for 32 KB, then copy
@@ -253,8 +271,8 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
 }
 
 struct Shared {
-  uint64_t w_full[kWStages], w_empty[kWStages];
-  uint64_t full[kStages], empty[kStages];   // X (TMA bytes) + A (4 dequant warps) of a k-step
+  uint64_t w_full[kMaxWStages], w_empty[kMaxWStages];
+  uint64_t full[kStages], empty[kStages];   // X (TMA bytes) + A (8 dequant warps) of a k-step
   uint64_t acc_full[kAccs], acc_empty[kAccs];
   uint64_t drain;
   uint64_t staged;          // epilogue warps that have staged their rows of the last tile
@@ -351,6 +369,35 @@ __device__ __forceinline__ void dequant_half(uint32_t codes, uint32_t scales, in
     }
   }
 }
+// Q8: columns [128 qh, 128 qh + 128) of weight row r of one chunk, as 64
+// bf16x2 words in k order: w = d*code, computed exactly in fp32 and rounded
+// once to bf16.  Code (r, k) is byte k*32 + r (layout KR) or
+// (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16 (layout BLK); the warp's 32
+// lanes read 32 rows of one column together.  Plain C++ loads: they stay
+// behind the stage's barrier wait (an asm statement with a memory clobber).
+template <int KIND>
+__device__ __forceinline__ void dequant_half_q8(const uint8_t* chunk, int r, int qh, uint32_t (&out)[64]) {
+  const uint2 dw = *reinterpret_cast<const uint2*>(chunk + kQ8D + r * 16 + qh * 8);   // d of groups 4qh .. 4qh+3
+  const uint8_t* c = chunk + (KIND == kQ8_KR ? r + qh * (128 * 32) : (r >> 4) * 4096 + (r & 15) + qh * (4 * 512));
+  const float2 kBias = make_float2(-8388736.f, -8388736.f);   // 2^23 + 128
+#pragma unroll
+  for (int gg = 0; gg < 4; ++gg) {
+    const uint32_t dp = gg < 2 ? dw.x : dw.y;
+    const float d = __uint_as_float((gg & 1) ? (dp & 0xFFFF0000u) : (dp << 16));
+    const float2 d2 = make_float2(d, d);
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const int k = 32 * gg + 2 * p;                // column within the half
+      const int o0 = KIND == kQ8_KR ? k * 32 : (k >> 5) * 512 + (k & 31) * 16;
+      const int o1 = KIND == kQ8_KR ? (k + 1) * 32 : ((k + 1) >> 5) * 512 + ((k + 1) & 31) * 16;
+      const uint32_t u0 = c[o0], u1 = c[o1];
+      // int8 code -> exact fp32: the bits 0x4B000000 | (u ^ 0x80) are 2^23 + 128 + code
+      const float2 f = make_float2(__uint_as_float((u0 ^ 0x80u) | 0x4B000000u), __uint_as_float((u1 ^ 0x80u) | 0x4B000000u));
+      const float2 w = __fmul2_rn(fadd2(f, kBias), d2);
+      out[16 * gg + p] = pack_bf16x2(w.x, w.y);
+    }
+  }
+}
 // 32 consecutive TMEM columns of this thread's lane <- r[0..31]; in flight on
 // return (tcgen05.wait::st completes it).
 __device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t* r) {
@@ -364,13 +411,16 @@ __device__ __forceinline__ void tmem_st32_async(uint32_t taddr, const uint32_t* 
       : "memory");
 }
 
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q41_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
+    gemm_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap smap,
                     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
                     const __grid_constant__ Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Shared* sh = reinterpret_cast<Shared*>(smem + kBarOff);
+  using P = Plan<KIND>;
+  constexpr int kWStages = P::kWStages, kWBytes = P::kWBytes, kXOff = P::kXOff;
+  Shared* sh = reinterpret_cast<Shared*>(smem + P::kBarOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t lo = a.units * blockIdx.x / a.grid, hi = a.units * (blockIdx.x + 1) / a.grid;
   const int n = static_cast<int>(hi - lo);
@@ -380,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;");
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantPerStep); }
-    for (int s = 0; s < kStages; ++s) { mbar_init(&sh->full[s], 1 + kDequantPerStep); mbar_init(&sh->empty[s], 1); }
+    for (int s = 0; s < kWStages; ++s) { mbar_init(&sh->w_full[s], 1); mbar_init(&sh->w_empty[s], kDequantWarps); }
+    for (int s = 0; s < kStages; ++s) { mbar_init(&sh->full[s], 1 + kDequantWarps); mbar_init(&sh->empty[s], 1); }
     for (int s = 0; s < kAccs; ++s) { mbar_init(&sh->acc_full[s], 1); mbar_init(&sh->acc_empty[s], 4); }
     mbar_init(&sh->drain, 1);
     mbar_init(&sh->staged, 4);
@@ -407,8 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; j < n; ++j) {
       const int s = j % kWStages;
       if (!wait_bar_warp(sh, &sh->w_empty[s], ((j / kWStages) & 1) ^ 1u, a.err)) break;
-      issue_weights(smem_u32(smem + kWOff + s * kWBytes), &wmap, &smap, static_cast<int>(ks), static_cast<int>(tile * 4),
-                    smem_u32(&sh->w_full[s]));
+      if (P::kQ8)
+        issue_weights_q8(smem_u32(smem + kWOff + s * kWBytes), &wmap, static_cast<int>(ks), static_cast<int>(tile * 4),
+                         smem_u32(&sh->w_full[s]));
+      else
+        issue_weights(smem_u32(smem + kWOff + s * kWBytes), &wmap, &smap, static_cast<int>(ks), static_cast<int>(tile * 4),
+                      smem_u32(&sh->w_full[s]));
       if (++ks == KS) { ks = 0; ++tile; }
     }
     for (int t = (j > kWStages ? j - kWStages : 0); t < j; ++t)        // copies still in flight land first
@@ -459,53 +513,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(&sh->drain, 0, 100000000ull);
   } else if (warp >= kWarpDequant0 && warp < kWarpEpi0) {
     // ----------------------------------------------------------- dequant
-    // Software-pipelined: the TMEM stores of a k-step stay in flight while the
-    // warp decodes its next k-step; only then are they completed and
-    // announced.  The barriers a step needs are tested (without blocking) one
-    // step ahead, so the round trip of the test overlaps the decode; a step
-    // blocks only if its stage is really not ready.
-    const int i = warp & 3, par = (warp - kWarpDequant0) >> 2;  // tile row (= TMEM lane quarter), k-step parity
+    // Software-pipelined: the TMEM stores of k-step j stay in flight while
+    // k-step j + 1 is decoded; only then are they completed and announced.
+    // The barriers a step needs are tested (without blocking) one step ahead,
+    // so the round trip of the test overlaps the decode; a step blocks only if
+    // its stage is really not ready.  Every dequant warp takes part in every
+    // k-step, so the stage a test looks at was last used by the same warp:
+    // the phase it tests is the next one, never an older one.
+    const int i = warp & 3, qh = (warp - kWarpDequant0) >> 2;   // tile row (= TMEM lane quarter), half of the k-step
     const uint32_t t_lane = static_cast<uint32_t>(32 * i) << 16;
-    int pst = -1;                                   // stage stored but not yet announced
-    // this warp's k-steps j = par, par + 2, ...: A/X stage j % kStages with phase (j / kStages) & 1,
-    // weight stage j % kWStages with phase (j / kWStages) & 1
-    bool w_ok = par < n ? mbar_test_wait(&sh->w_full[par % kWStages], (par / kWStages) & 1) : true;
-    for (int j = par; j < n; j += 2) {
-      const int ws = j % kWStages, st = j % kStages;
-      const uint32_t wph = (j / kWStages) & 1, ph = (j / kStages) & 1;
+    int st = 0, pst = -1;                           // stage of this k-step, stage stored but not yet announced
+    uint32_t ph = 0;
+    int ws = 0;                                     // weight stage of this k-step
+    uint32_t wph = 0;
+    bool w_ok = mbar_test_wait(&sh->w_full[0], 0);
+    for (int j = 0; j < n; ++j) {
       if (!__all_sync(0xFFFFFFFFu, w_ok) && !wait_bar_warp(sh, &sh->w_full[ws], wph, a.err)) break;
-      const int jn = j + 2;
-      const bool w_ok_next = jn < n ? mbar_test_wait(&sh->w_full[jn % kWStages], (jn / kWStages) & 1) : true;
+      const int ws_next = ws + 1 == kWStages ? 0 : ws + 1;
+      const uint32_t wph_next = ws + 1 == kWStages ? wph ^ 1u : wph;
+      const bool w_ok_next = j + 1 < n ? mbar_test_wait(&sh->w_full[ws_next], wph_next) : true;
       const bool e_ok = mbar_test_wait(&sh->empty[st], ph ^ 1u);
-      const uint32_t wst = smem_u32(smem + kWOff + ws * kWBytes);
-      const uint32_t tdst = tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols;
+      uint32_t out[64];
       // (the last tile may hold fewer than 4 tile rows: the rows past the end
       // decode whatever the stage holds, and their results are never stored)
-#pragma unroll 1
-      for (int qh = 0; qh < 2; ++qh) {
-        uint32_t out[64];
+      if constexpr (P::kQ8) {
+        dequant_half_q8<KIND>(smem + kWOff + ws * kWBytes + i * kQ8Bytes, lane, qh, out);
+      } else {
+        const uint32_t wst = smem_u32(smem + kWOff + ws * kWBytes);
         dequant_half(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qh, out);
-        if (qh == 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->w_empty[ws]);   // the stage's bytes are in registers
-        }
-        if (pst >= 0) {                             // the previous k-step's stores, completed and announced
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->full[pst]);
-          pst = -1;
-        }
-        if (qh == 0 && !__all_sync(0xFFFFFFFFu, e_ok) && !wait_bar_warp(sh, &sh->empty[st], ph ^ 1u, a.err)) {
-          pst = -2;                                 // give up (error path)
-          break;
-        }
-        tc_fence_after();
-        tmem_st32_async(tdst + static_cast<uint32_t>(qh * 64), out);
-        tmem_st32_async(tdst + static_cast<uint32_t>(qh * 64 + 32), out + 32);
       }
-      if (pst == -2) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->w_empty[ws]); // the stage's bytes are in registers
+      if (pst >= 0) {
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->full[pst]);
+        pst = -1;
+      }
+      if (!__all_sync(0xFFFFFFFFu, e_ok) && !wait_bar_warp(sh, &sh->empty[st], ph ^ 1u, a.err)) break;
+      tc_fence_after();
+      const uint32_t tdst = tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols + static_cast<uint32_t>(qh * 64);
+      tmem_st32_async(tdst, out);
+      tmem_st32_async(tdst + 32, out + 32);
       pst = st;
+      if (++st == kStages) { st = 0; ph ^= 1u; }
+      ws = ws_next;
+      wph = wph_next;
       w_ok = w_ok_next;
     }
     if (pst >= 0) {
@@ -679,7 +733,7 @@ EncodeTiled encode_fn() {
 }
 }  // namespace
 
-bool gemm_supports(int kind) { return kind == kQ4_1; }
+bool gemm_supports(int kind) { return kind == kQ4_1 || kind == kQ8_KR || kind == kQ8_BLK; }
 
 uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M) {
   (void)TC;
@@ -690,39 +744,49 @@ uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M) {
          static_cast<uint64_t>(1024) * gemm::kTileN * gemm::kTileM * 4;
 }
 
-cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, const void* X, int M, void* Y,
-                        int out_f32, void* workspace, cudaStream_t s) {
-  if (kind != kQ4_1) return cudaErrorNotSupported;
-  EncodeTiled enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  DeviceInfo info;
-  cudaError_t e = device_info(&info);
-  if (e != cudaSuccess) return e;
-  if (info.max_smem_optin < gemm::kSmemBytes) return cudaErrorNotSupported;
-
-  // weights: code regions as [128 B][32 rows][TC chunk columns][TR tile rows] (128-byte swizzle) and
-  // scale/zero regions as [256 B][4][TC][TR] from byte 4096 of each chunk; X as [64 k][M tokens][K / 64]
+namespace {
+template <int KIND>
+cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void* chunks, int64_t TR, int64_t TC,
+                             const void* X, int M, void* Y, int out_f32, void* workspace, cudaStream_t s) {
+  using P = gemm::Plan<KIND>;
+  if (info.max_smem_optin < P::kSmemBytes) return cudaErrorNotSupported;
+  // weights, q4_1: code regions as [128 B][32 rows][TC chunk columns][TR tile rows] (128-byte swizzle)
+  // and scale/zero regions as [256 B][4][TC][TR] from byte 4096 of each chunk; Q8: whole chunks as
+  // [256 B][34][TC][TR].  X as [64 k][M tokens][K / 64]; Y as [N][M].
   CUtensorMap wmap, smap, xmap, ymap;
-  {
-    cuuint64_t dims[4] = {128, 32, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
-    cuuint64_t strides[3] = {128, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
-    cuuint32_t box[4] = {128, 32, 1, 4};
+  if (P::kQ8) {
+    cuuint64_t dims[4] = {256, kQ8Bytes / 256, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
+    cuuint64_t strides[3] = {256, kQ8Bytes, static_cast<cuuint64_t>(kQ8Bytes) * static_cast<cuuint64_t>(TC)};
+    cuuint32_t box[4] = {256, kQ8Bytes / 256, 1, 4};
     cuuint32_t es[4] = {1, 1, 1, 1};
+    static_assert(kQ8Bytes % 256 == 0, "Q8 chunk as rows of 256 bytes");
     if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(chunks), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[4] = {256, 4, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
-    cuuint64_t strides[3] = {256, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
-    cuuint32_t box[4] = {256, 4, 1, 4};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(chunks) + kQ41Scale);
-    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    smap = wmap;                                    // unused for Q8
+  } else {
+    {
+      cuuint64_t dims[4] = {128, 32, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
+      cuuint64_t strides[3] = {128, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
+      cuuint32_t box[4] = {128, 32, 1, 4};
+      cuuint32_t es[4] = {1, 1, 1, 1};
+      if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(chunks), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    {
+      cuuint64_t dims[4] = {256, 4, static_cast<cuuint64_t>(TC), static_cast<cuuint64_t>(TR)};
+      cuuint64_t strides[3] = {256, kQ41Bytes, static_cast<cuuint64_t>(kQ41Bytes) * static_cast<cuuint64_t>(TC)};
+      cuuint32_t box[4] = {256, 4, 1, 4};
+      cuuint32_t es[4] = {1, 1, 1, 1};
+      void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(chunks) + kQ41Scale);
+      if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
   }
   {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(TC * 4)};
@@ -766,21 +830,37 @@ cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, co
   if (grid > 1024) grid = 1024;
   if (grid < 1) grid = 1;
   a.grid = static_cast<int>(grid);
-  e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm::gemm_q41_kernel), 16);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm::gemm_kernel<KIND>), 16 + KIND);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(gemm::kThreads);
-  cfg.dynamicSmemBytes = gemm::kSmemBytes;
+  cfg.dynamicSmemBytes = P::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm::gemm_q41_kernel, wmap, smap, xmap, ymap, a);
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<KIND>, wmap, smap, xmap, ymap, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm(int kind, const void* chunks, int64_t TR, int64_t TC, const void* X, int M, void* Y,
+                        int out_f32, void* workspace, cudaStream_t s) {
+  if (!gemm_supports(kind)) return cudaErrorNotSupported;
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  DeviceInfo info;
+  cudaError_t e = device_info(&info);
+  if (e != cudaSuccess) return e;
+  switch (kind) {
+    case kQ4_1: return launch_gemm_kind<kQ4_1>(enc, info, chunks, TR, TC, X, M, Y, out_f32, workspace, s);
+    case kQ8_KR: return launch_gemm_kind<kQ8_KR>(enc, info, chunks, TR, TC, X, M, Y, out_f32, workspace, s);
+    default: return launch_gemm_kind<kQ8_BLK>(enc, info, chunks, TR, TC, X, M, Y, out_f32, workspace, s);
+  }
 }
 
 }  // namespace q4nx

@@ -129,10 +129,13 @@ uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
 /* Fused decode + GEMM for a block of 1..64 tokens on the tcgen05 tensor cores:
  *   Y[m][n] = sum_k X[m][k] * w[n][k],  m < M.
  * X_dev: bf16 [M][cols] row-major.  Y_dev: [M][rows] row-major of out_dtype.
- * Weights are decoded to bf16 in shared memory and multiplied with fp32
- * accumulation in tensor memory.  Kind: q4_1.  Q4_K returns Q4NX_E_UNSUPPORTED
- * (repack it with q4nx_repack_q4k first, which keeps the codes); so do the Q8
- * kinds in this version.
+ * Weights are decoded to bf16 (code*scale + zero for q4_1, rounded once; d*code
+ * for Q8, exactly the standalone decode) into tensor memory and multiplied with
+ * fp32 accumulation there.  Kinds: q4_1, Q8_KR, Q8_BLK.  Q4_K returns
+ * Q4NX_E_UNSUPPORTED (repack it with q4nx_repack_q4k first, which keeps the
+ * codes).  The launch expects its CTAs (at most one per SM) to be resident
+ * together, as they are when no other kernel occupies the GPU; a stalled
+ * launch gives up after a bounded wait and reports it through q4nx_check.
  * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes, zero-filled before
  * first use (it holds the error word). */
 int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, int out_dtype,

@@ -1,9 +1,12 @@
-"""Parity of the tensor-core decode + GEMM (q4nx_gemm_m64) with the oracle.
+"""Parity of the tensor-core decode + GEMM (q4nx_gemm_m64) with the oracle, for
+q4_1 chunks and Q8 chunks in both code layouts.
 
 Bar: every output within 1e-3 * sum_k |w_k x_k| of the binary64 oracle (plus
 2^-8 |y| for bf16 outputs), per-row cosine >= 0.99999.  The kernel multiplies
 bf16-decoded weights with fp32 accumulation on tcgen05 tensor cores.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -92,3 +95,37 @@ def test_gemm_matches_gemv_per_token(q):
     for m in range(M):
         y = out_values(q.q4nx_gemv(W, Xd[m].contiguous(), out_dtype="f32"))
         assert np.all(np.abs(Y[m] - y) <= 2e-3 * A[m])
+
+
+# ---- Q8 chunks (both code layouts): w = d * code, the lm_head kind ----
+
+@pytest.mark.parametrize("kind", [synth.Q8_KR, synth.Q8_BLK])
+@pytest.mark.parametrize("N,K", [(128, 512), (256, 1024), (4224, 512), (160, 2816)])
+@pytest.mark.parametrize("M", [64, 1, 17])
+def test_gemm_q8_small(q, kind, N, K, M):
+    run(q, kind, N, K, M, wid=5)
+
+
+@pytest.mark.parametrize("kind", [synth.Q8_KR, synth.Q8_BLK])
+def test_gemm_q8_bf16_output(q, kind):
+    run(q, kind, 512, 1536, 64, out="bf16", wid=5)
+
+
+@pytest.mark.parametrize("kind", [synth.Q8_KR, synth.Q8_BLK])
+def test_gemm_q8_lm_head_64_tokens(q, kind):
+    """The Q8 lm_head 151936x2560 at 64 tokens, fp32 logits (rows sampled for the oracle)."""
+    N, K = 151936, 2560
+    rows = np.unique(np.concatenate([np.arange(0, 160), np.arange(N - 160, N),
+                                     np.random.default_rng(5).integers(0, N, 600)]))
+    run(q, kind, N, K, 64, out="f32", rows=rows, wid=5)
+
+
+def test_gemm_q8_layouts_agree_on_the_same_weights(q):
+    """The same logical codes packed in layout KR and in layout BLK give the same products, bit for bit."""
+    N, K, M = 512, 2048, 64
+    f, wkr = synth.make(synth.Q8_KR, N, K, synth.rng(5, 0, 95))
+    wblk = synth.pack(dataclasses.replace(f, kind=synth.Q8_BLK))
+    X = to_dev_bf16(synth.activations(synth.rng(5, 0, 96), M, K))
+    a = q.q4nx_gemm_m64(q.Weight(to_dev_bytes(wkr), synth.Q8_KR, N, K), X, out_dtype="f32")
+    b = q.q4nx_gemm_m64(q.Weight(to_dev_bytes(wblk), synth.Q8_BLK, N, K), X, out_dtype="f32")
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
