@@ -18,6 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_smem[kMaxDevices];
+std::atomic<int> g_smem_pair[kMaxDevices];
 // one flag per (device, kernel slot) that the max dynamic smem attribute was set
 std::atomic<uint32_t> g_attr_set[kMaxDevices];
 }  // namespace
@@ -29,16 +30,27 @@ cudaError_t device_info(DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   int sms = g_sms[dev].load(std::memory_order_relaxed);
   int smem = g_smem[dev].load(std::memory_order_relaxed);
-  if (sms <= 0 || smem <= 0) {
+  int pair = g_smem_pair[dev].load(std::memory_order_relaxed);
+  if (sms <= 0 || smem <= 0 || pair <= 0) {
+    int per_sm = 0, reserved = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    pair = per_sm / 2 - reserved;
+    if (pair > smem) pair = smem;
+    if (pair < 1) pair = 1;
     g_sms[dev].store(sms, std::memory_order_relaxed);
     g_smem[dev].store(smem, std::memory_order_relaxed);
+    g_smem_pair[dev].store(pair, std::memory_order_relaxed);
   }
   out->sms = sms;
   out->max_smem_optin = smem;
+  out->smem_two_per_sm = pair;
   return cudaSuccess;
 }
 
@@ -168,8 +180,8 @@ int q4nx_gemv_batch(const q4nx_gemv_item* items, int count, int out_dtype, void*
   if (!aligned16(workspace_dev)) return Q4NX_E_ALIGN;
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return Q4NX_E_CUDA;
-  return from_cuda(launch_gemv_batch(items[0].w.kind, it, count, out_dtype == Q4NX_OUT_F32, workspace_dev, info.sms,
-                                     info.max_smem_optin, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemv_batch(items[0].w.kind, it, count, out_dtype == Q4NX_OUT_F32, workspace_dev, info,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype, void* workspace_dev,

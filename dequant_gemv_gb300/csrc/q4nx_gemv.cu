@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   uint32_t* cnt = reinterpret_cast<uint32_t*>(slots + nwarps * 64);         // [nwarps][2]
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
-  Pos cur, pre;                             // chunk being processed / next chunk to fetch
+  Pos cur{}, pre{};                         // chunk being processed / next chunk to fetch
   cur.seek(a, lo);
   pre = cur;
   if (lane == 0) {
@@ -475,26 +475,35 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
 
 // ----------------------------------------------------------------- host ----
 
-bool gemv_plan(int kind, int64_t T, int sms, int max_smem, GemvPlan* p) {
+bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
   const int CB = chunk_bytes_of(kind);
-  if (CB == 0 || sms <= 0 || T <= 0) return false;
+  if (CB == 0 || info.sms <= 0 || T <= 0) return false;
   const uint64_t SB = static_cast<uint64_t>(CB) + kXSliceBytes;
-  static const int kWarpChoices[] = {16, 12, 8, 6, 4, 2, 1};
   auto need = [&](int w, int st) {
     return static_cast<uint64_t>(w) * st * SB + align16(static_cast<uint64_t>(w) * st * 8) +
            static_cast<uint64_t>(w) * (kScratchBytes + kSlotBytes);
   };
+  // Eight warps per CTA, each streaming a longer run of chunks, measured best
+  // on GB300 against 12 and 16.  4-bit chunks: the CTA stays within half an
+  // SM's shared memory, so that the next launch in the stream (programmatic
+  // dependent launch) starts its weight copies on the same SMs while this one
+  // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
+  // chunks are larger and gain more from a deeper ring than from that overlap.
+  const uint64_t cap = static_cast<uint64_t>(CB <= kQ41Bytes ? info.smem_two_per_sm : info.max_smem_optin);
+  static const int kWarpChoices[] = {8, 6, 4, 2, 1};
   int warps = 0, stages = 0;
   for (int w : kWarpChoices) {
-    if (need(w, 2) <= static_cast<uint64_t>(max_smem)) { warps = w; stages = 2; break; }
+    for (int st = 4; st >= 2; --st) {
+      if (need(w, st) <= cap) { warps = w; stages = st; break; }
+    }
+    if (warps) break;
   }
   if (!warps) return false;
-  if (need(warps, 3) <= static_cast<uint64_t>(max_smem)) stages = 3;
   // One CTA per SM; small problems use fewer CTAs of at least ~4 chunks each so
   // that split tile rows are combined inside a CTA rather than across CTAs.
   int64_t grid = T / 4;
   if (grid < 1) grid = 1;
-  if (grid > sms) grid = sms;
+  if (grid > info.sms) grid = info.sms;
   if (grid > kMaxCtas) grid = kMaxCtas;
   const int64_t per_cta = T / grid;                // every warp gets at least one chunk
   if (per_cta < warps) warps = static_cast<int>(per_cta);
@@ -534,8 +543,8 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
 }
 
 template <int MAXB>
-static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
-                                     int max_smem, cudaStream_t s) {
+static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
+                                     const DeviceInfo& info, cudaStream_t s) {
   GemvArgsT<MAXB> a;
   int64_t T = 0, TRsum = 0;
   for (int i = 0; i < n; ++i) {
@@ -550,7 +559,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
     TRsum += items[i].TR;
   }
   GemvPlan p;
-  if (!gemv_plan(kind, T, sms, max_smem, &p)) return cudaErrorInvalidValue;
+  if (!gemv_plan(kind, T, info, &p)) return cudaErrorInvalidValue;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.nitems = n;
   a.grid = p.grid;
@@ -569,12 +578,12 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   }
 }
 
-cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
-                              int max_smem, cudaStream_t s) {
+cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
+                              const DeviceInfo& info, cudaStream_t s) {
   if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
-  if (n == 1) return launch_gemv_sized<1>(kind, items, n, out_f32, workspace, sms, max_smem, s);
-  if (n <= 8) return launch_gemv_sized<8>(kind, items, n, out_f32, workspace, sms, max_smem, s);
-  return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, sms, max_smem, s);
+  if (n == 1) return launch_gemv_sized<1>(kind, items, n, out_f32, workspace, info, s);
+  if (n <= 8) return launch_gemv_sized<8>(kind, items, n, out_f32, workspace, info, s);
+  return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, info, s);
 }
 
 }  // namespace q4nx

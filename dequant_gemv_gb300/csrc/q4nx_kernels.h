@@ -9,7 +9,8 @@ namespace q4nx {
 
 struct DeviceInfo {
   int sms = 0;
-  int max_smem_optin = 0;
+  int max_smem_optin = 0;      // dynamic shared memory one CTA may opt in to
+  int smem_two_per_sm = 0;     // the most dynamic shared memory a CTA may use with two CTAs on one SM
 };
 // Properties of the current device (cached per device ordinal).
 cudaError_t device_info(DeviceInfo* out);
@@ -32,10 +33,10 @@ struct GemvPlan {
   int grid = 0;        // CTAs, each owning a contiguous range of chunks
   size_t smem = 0;     // dynamic shared memory bytes
 };
-bool gemv_plan(int kind, int64_t total_chunks, int sms, int max_smem, GemvPlan* plan);
+bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan);
 uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks);
-cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace, int sms,
-                              int max_smem, cudaStream_t s);
+cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
+                              const DeviceInfo& info, cudaStream_t s);
 
 // ---- standalone decode ----
 cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s);

@@ -81,7 +81,7 @@ int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int 
   item.y = y_dev;
   item.TR = TR;
   item.TC = TC;
-  return launch_gemv_batch(w->kind, &item, 1, out_dtype == Q4NX_OUT_F32, scratch, info.sms, info.max_smem_optin, s) ==
+  return launch_gemv_batch(w->kind, &item, 1, out_dtype == Q4NX_OUT_F32, scratch, info, s) ==
                  cudaSuccess
              ? Q4NX_OK
              : Q4NX_E_CUDA;
