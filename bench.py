@@ -184,6 +184,24 @@ def run_reference(args, rank: int):
 
 # ----------------------------------------------------------------- GPU arm --
 
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The largest of every rank's v (each rank's own v when world == 1)."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, bytes_per_rank_step: float, steps: int, seconds: float) -> float:
+    """Whole-job GB/s: every rank streams its own copy of the step (weak scaling),
+    timed by the slowest rank."""
+    return world * bytes_per_rank_step * steps / seconds / 1e9
+
+
 def run_gpu(args, rank: int, world: int):
     import torch
 
@@ -276,13 +294,9 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = ms / args.steps
-    value = world * wtot * args.steps / (ms / 1e3) / 1e9
+    value = job_throughput(world, wtot, args.steps, ms / 1e3)
 
     # other schedules of the same step, for context (not the headline)
     def time_graph(g, n):
@@ -327,11 +341,8 @@ def run_gpu(args, rank: int, world: int):
             y_host.copy_(ydev, non_blocking=True)
             stream.synchronize()
         t_e2e = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e_value = world * wtot * e2e_steps / t_e2e / 1e9
+    t_e2e = max_over_ranks(t_e2e, world, dev)
+    e2e_value = job_throughput(world, wtot, e2e_steps, t_e2e)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
