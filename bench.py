@@ -461,6 +461,17 @@ def run_suite(args):
             emit({"suite": "gemv", "workload": name, "M": 1, "us": us, "weight_gbs": nb / us / 1e3,
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm},
                   "frac_of_nominal_8tbs": nb / us / 1e3 / 8000.0, "copies": R})
+        if wid == 5 and want("top1"):
+            # lm_head GEMV fused with top-1 (logits never written) vs the GEMV then the argmax kernel
+            idx1 = torch.empty(1, dtype=torch.int32, device=dev)
+            yl = torch.empty((1, N), dtype=torch.float32, device=dev)
+            us_f = timeit([lambda W=W: q.q4nx_gemv_top1(W, x, out=idx1, ws=ws) for W in Ws], 400)
+            us_s = timeit([lambda W=W: (q.q4nx_gemv(W, x, out=yl[0], out_dtype="f32", ws=ws),
+                                        q.q4nx_argmax(yl, out=idx1)) for W in Ws], 400)
+            alg = nb + 2 * K + 4
+            emit({"suite": "gemv_top1", "workload": name, "M": 1, "us": us_f, "us_gemv_then_argmax": us_s,
+                  "weight_gbs": nb / us_f / 1e3,
+                  "roofline": {"bound": "hbm", "achieved": alg / us_f / 1e3, "peak": hbm, "frac": alg / us_f / 1e3 / hbm}})
         if wid in (1, 5) and want("decode"):
             outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(min(R, 2))]
             us = timeit([lambda W=W, o=outs[i % len(outs)]: q.q4nx_decode(W, out=o) for i, W in enumerate(Ws)], 64)
@@ -512,7 +523,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
-    ap.add_argument("--only", default="", help="suite: comma list of gemv,decode,repack,gemm_m64,argmax")
+    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,gemm_m64,argmax")
     ap.add_argument("--case", default="", help="suite: substring of the workload name")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -68,6 +68,7 @@ def _load():
         "q4nx_decode": ([W, P, U64, P], I),
         "q4nx_gemv": ([W, P, P, I, P, U64, P], I),
         "q4nx_gemv_workspace": ([W], U64),
+        "q4nx_gemv_top1": ([W, P, P, P, U64, P], I),
         "q4nx_gemv_batch": ([ctypes.POINTER(q4nx_gemv_item), I, I, P, U64, P], I),
         "q4nx_gemv_batch_workspace": ([ctypes.POINTER(q4nx_gemv_item), I], U64),
         "q4nx_gemm_m64": ([W, P, I, P, I, P, U64, P], I),
@@ -87,7 +88,7 @@ def _load():
 
 lib = _load()
 EXPORTS = ("q4nx_chunk_bytes", "q4nx_status_str", "q4nx_abi_version", "q4nx_decode", "q4nx_gemv",
-           "q4nx_gemv_workspace", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_argmax",
+           "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_argmax",
            "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes")
 
 
@@ -193,6 +194,26 @@ def q4nx_gemv(w: Weight, x: torch.Tensor, out: torch.Tensor | None = None, out_d
             ws = workspace(w.device, need)
         _check(lib.q4nx_gemv(ctypes.byref(cw), x.data_ptr(), out.data_ptr(), code, ws.data_ptr(),
                              ws.numel(), _stream(w.device)), "q4nx_gemv")
+    return out
+
+
+def q4nx_gemv_top1(w: Weight, x: torch.Tensor, out: torch.Tensor | None = None,
+                   ws: torch.Tensor | None = None) -> torch.Tensor:
+    """int32 [1]: the row of the largest fp32 output of w @ x (lowest row on ties; a NaN wins)."""
+    _cuda(w.chunks, "chunks")
+    _cuda(x, "x")
+    if x.dtype != torch.bfloat16 or x.numel() != w.cols:
+        raise ValueError("x must be bf16 with cols elements")
+    with torch.cuda.device(w.device):
+        if out is None:
+            out = torch.empty(1, dtype=torch.int32, device=w.device)
+        _cuda(out, "out")
+        cw = w.c()
+        need = int(lib.q4nx_gemv_workspace(ctypes.byref(cw)))
+        if ws is None:
+            ws = workspace(w.device, need)
+        _check(lib.q4nx_gemv_top1(ctypes.byref(cw), x.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                  _stream(w.device)), "q4nx_gemv_top1")
     return out
 
 

@@ -54,8 +54,9 @@ cudaError_t device_info(DeviceInfo* out) {
   return cudaSuccess;
 }
 
-// Raise a kernel's dynamic shared-memory limit to the device maximum, once per
-// (device, slot).  Slots 0..31 are free for the kernels to use.
+// Raise a kernel's dynamic shared-memory limit to the device maximum (less the
+// kernel's static shared memory), once per (device, slot).  Slots 0..31 are
+// free for the kernels to use.
 cudaError_t set_max_dynamic_smem(const void* func, int slot) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -66,7 +67,13 @@ cudaError_t set_max_dynamic_smem(const void* func, int slot) {
   DeviceInfo info;
   e = device_info(&info);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, info.max_smem_optin);
+  // the opt-in limit covers static and dynamic shared memory together
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  const int dyn = info.max_smem_optin - static_cast<int>(fa.sharedSizeBytes);
+  if (dyn <= 0) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   g_attr_set[dev].fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
@@ -194,6 +201,26 @@ int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtyp
   item.x_dev = x_dev;
   item.y_dev = y_dev;
   return q4nx_gemv_batch(&item, 1, out_dtype, workspace_dev, workspace_bytes, stream);
+}
+
+int q4nx_gemv_top1(const q4nx_weight* w, const void* x_dev, int32_t* idx_dev, void* workspace_dev,
+                   uint64_t workspace_bytes, void* stream) {
+  int st = check_weight(w);
+  if (st) return st;
+  if (x_dev == nullptr || idx_dev == nullptr) return Q4NX_E_NULL;
+  if (!aligned16(x_dev) || (reinterpret_cast<uintptr_t>(idx_dev) & 3u)) return Q4NX_E_ALIGN;
+  const int64_t TR = w->rows / 32, TC = w->cols / 256;
+  if (workspace_dev == nullptr || workspace_bytes < gemv_workspace_bytes(TR, TR * TC)) return Q4NX_E_WORKSPACE;
+  if (!aligned16(workspace_dev)) return Q4NX_E_ALIGN;
+  DeviceInfo info;
+  if (device_info(&info) != cudaSuccess) return Q4NX_E_CUDA;
+  GemvItem item;
+  item.chunks = w->chunks_dev;
+  item.x = x_dev;
+  item.y = nullptr;
+  item.TR = TR;
+  item.TC = TC;
+  return from_cuda(launch_gemv_top1(w->kind, item, idx_dev, workspace_dev, info, static_cast<cudaStream_t>(stream)));
 }
 
 uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M) {

@@ -207,4 +207,23 @@ __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Top-1 key: (value, index) -> 64 bits whose unsigned order is the wanted
+// order: NaN above +inf above every number, +0 == -0, and for equal values
+// the lower index above (so a maximum picks the first NaN, else the first of
+// the largest values).  Key 0 is below every key of a real value.
+__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
+  uint32_t ord;
+  if (v != v) {
+    ord = 0xFFFFFFFFu;
+  } else {
+    uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+    ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(~idx);
+}
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ int32_t argmax_index(uint64_t key) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(key & 0xFFFFFFFFu));
+}
+
 }  // namespace q4nx

@@ -65,7 +65,15 @@ struct GemvArgsT {
   uint32_t* err;
   uint32_t* counters;      // [sum TR]
   float* partials;         // [grid][2][32]: a CTA's first and last tile row when other CTAs share them
+  // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
+  // row) key; the last CTA to finish writes the row index
+  int32_t* top1_idx;       // null: store y
+  uint64_t* top1_key;      // workspace word, zero between launches
+  uint32_t* top1_done;     // workspace word, zero between launches
 };
+
+// This CTA's largest top-1 key so far (top-1 mode).
+__shared__ unsigned long long s_top1_key;
 
 // Lane-wise transpose-reduce of 8 values over the 8 lanes selected by masks
 // (m2, m1, m0): afterwards the lane whose mask bits read (b2 b1 b0) holds the
@@ -92,8 +100,17 @@ __device__ __forceinline__ float transpose_reduce8(float v[8], int lane, int m2,
 // CTA that holds chunk c: the largest b with floor(T*b/G) <= c
 __device__ __forceinline__ int64_t cta_of(int64_t c, int64_t T, int64_t G) { return ((c + 1) * G - 1) / T; }
 
+// Row n's final value (called by all 32 lanes of a warp together, one row
+// each): store it, or in top-1 mode fold it into the CTA's largest key.
 template <class GemvArgs>
 __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, float v) {
+  if (a.top1_idx) {
+    uint64_t key = argmax_key(v, static_cast<uint32_t>(n));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(&s_top1_key, static_cast<unsigned long long>(key));
+    return;
+  }
   if (a.out_f32) static_cast<float*>(y)[n] = v;
   else static_cast<uint16_t*>(y)[n] = f32_to_bf16_bits(v);
 }
@@ -426,6 +443,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     }
   }
   if (lane < 2) cnt[warp * 2 + lane] = 0u;
+  if (threadIdx.x == 0) s_top1_key = 0ull;
   __syncwarp();
   __syncthreads();                          // the row counters are zero before any warp can count
 
@@ -471,6 +489,22 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     const float v = finish_rows<KIND>(yacc, lane, row);
     finish_segment(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
   }
+  if (a.top1_idx) {
+    // every warp's rows are folded in; the CTA's key goes to the launch's key,
+    // and the last CTA to finish writes the index and clears the two words
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned long long k = s_top1_key;
+      if (k != 0ull) atomicMax(reinterpret_cast<unsigned long long*>(a.top1_key), k);
+      __threadfence();
+      if (atomicAdd(a.top1_done, 1u) == static_cast<uint32_t>(a.grid - 1)) {
+        __threadfence();
+        const unsigned long long best = atomicExch(reinterpret_cast<unsigned long long*>(a.top1_key), 0ull);
+        *a.top1_idx = argmax_index(best);
+        *a.top1_done = 0u;
+      }
+    }
+  }
 }
 
 // ----------------------------------------------------------------- host ----
@@ -489,7 +523,8 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
   // dependent launch) starts its weight copies on the same SMs while this one
   // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
   // chunks are larger and gain more from a deeper ring than from that overlap.
-  const uint64_t cap = static_cast<uint64_t>(CB <= kQ41Bytes ? info.smem_two_per_sm : info.max_smem_optin);
+  // (less 64 bytes for the kernel's static shared memory)
+  const uint64_t cap = static_cast<uint64_t>(CB <= kQ41Bytes ? info.smem_two_per_sm : info.max_smem_optin) - 64;
   static const int kWarpChoices[] = {8, 6, 4, 2, 1};
   int warps = 0, stages = 0;
   for (int w : kWarpChoices) {
@@ -544,7 +579,7 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
 
 template <int MAXB>
 static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
-                                     const DeviceInfo& info, cudaStream_t s) {
+                                     const DeviceInfo& info, int32_t* top1_idx, cudaStream_t s) {
   GemvArgsT<MAXB> a;
   int64_t T = 0, TRsum = 0;
   for (int i = 0; i < n; ++i) {
@@ -567,6 +602,9 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   a.out_f32 = out_f32;
   a.T = T;
   a.err = reinterpret_cast<uint32_t*>(ws);
+  a.top1_idx = top1_idx;
+  a.top1_done = reinterpret_cast<uint32_t*>(ws + 4);
+  a.top1_key = reinterpret_cast<uint64_t*>(ws + 8);
   a.counters = reinterpret_cast<uint32_t*>(ws + kWsErrBytes);
   a.partials = reinterpret_cast<float*>(ws + kWsErrBytes + align16(static_cast<uint64_t>(TRsum) * 4));
   switch (kind) {
@@ -581,9 +619,14 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                               const DeviceInfo& info, cudaStream_t s) {
   if (n < 1 || n > kMaxBatch) return cudaErrorInvalidValue;
-  if (n == 1) return launch_gemv_sized<1>(kind, items, n, out_f32, workspace, info, s);
-  if (n <= 8) return launch_gemv_sized<8>(kind, items, n, out_f32, workspace, info, s);
-  return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, info, s);
+  if (n == 1) return launch_gemv_sized<1>(kind, items, n, out_f32, workspace, info, nullptr, s);
+  if (n <= 8) return launch_gemv_sized<8>(kind, items, n, out_f32, workspace, info, nullptr, s);
+  return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, info, nullptr, s);
+}
+
+cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
+                             cudaStream_t s) {
+  return launch_gemv_sized<1>(kind, &item, 1, 1, workspace, info, idx, s);
 }
 
 }  // namespace q4nx

@@ -38,6 +38,12 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks);
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                               const DeviceInfo& info, cudaStream_t s);
 
+// GEMV of one item fused with top-1: *idx = the row of the largest fp32
+// output (ties: lowest row; a NaN output wins, the first one), y not written.
+// The workspace's bytes 4..15 hold the launch's top-1 words (zero between launches).
+cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
+                             cudaStream_t s);
+
 // ---- standalone decode ----
 cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s);
 

@@ -154,18 +154,6 @@ cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out,
 constexpr int kArgmaxCluster = 8;
 constexpr int kArgmaxThreads = 256;
 
-__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
-  uint32_t ord;
-  if (v != v) {
-    ord = 0xFFFFFFFFu;
-  } else {
-    uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
-    ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  }
-  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint32_t>(~idx);
-}
-
-__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
 __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
     argmax_kernel(const float* __restrict__ logits, int64_t V, int32_t* __restrict__ idx) {
@@ -210,7 +198,7 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
   if (rank == 0 && threadIdx.x == 0) {
     uint64_t b = 0;
     for (unsigned r = 0; r < kArgmaxCluster; ++r) b = umax64(b, *cluster.map_shared_rank(&cta_best, r));
-    idx[m] = static_cast<int32_t>(~static_cast<uint32_t>(b & 0xFFFFFFFFu));
+    idx[m] = argmax_index(b);
   }
   cluster.sync();      // peers keep their shared memory until rank 0 has read it
 }

@@ -107,6 +107,17 @@ int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtyp
               void* workspace_dev, uint64_t workspace_bytes, void* stream);
 uint64_t q4nx_gemv_workspace(const q4nx_weight* w);
 
+/* lm_head GEMV fused with top-1 (greedy decoding: the serving section of the
+ * "NPU engine" page and onw's TECHNICAL.md take only the argmax of the logits):
+ * *idx_dev = argmax over n of y[n], y = w * x_dev computed exactly as
+ * q4nx_gemv with Q4NX_OUT_F32 computes it.  Ties go to the lowest row; a NaN
+ * output wins (the first one).  The logits are never written to memory.
+ * idx_dev: device int32, 4-byte aligned.  Workspace: q4nx_gemv_workspace(w)
+ * bytes under the same zero-fill rule (the launch uses bytes 4..15 of it and
+ * leaves them zero). */
+int q4nx_gemv_top1(const q4nx_weight* w, const void* x_dev, int32_t* idx_dev, void* workspace_dev,
+                   uint64_t workspace_bytes, void* stream);
+
 /* One GEMV of a batch: y_dev[rows] = w * x_dev[cols]. */
 typedef struct q4nx_gemv_item {
     q4nx_weight w;

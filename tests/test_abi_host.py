@@ -80,6 +80,10 @@ def test_validation_statuses(q):
     assert L.q4nx_gemv(by(w), P, P, 0, None, need, None) == 7
     assert L.q4nx_gemv(by(w), P, P, 0, P, need - 1, None) == 7
     assert L.q4nx_gemv(by(w), P + 2, P, 0, P, need, None) == 5
+    # fused top-1: same weight checks; the index pointer needs 4-byte alignment
+    assert L.q4nx_gemv_top1(by(w), P, None, P, need, None) == 1
+    assert L.q4nx_gemv_top1(by(w), P, P + 2, P, need, None) == 5
+    assert L.q4nx_gemv_top1(by(w), P, P, P, need - 1, None) == 7
     assert L.q4nx_gemv_workspace(by(_w(q, rows=33))) == 0
     # gemv batch
     items = (q.q4nx_gemv_item * 3)()
