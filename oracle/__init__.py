@@ -20,6 +20,8 @@ decode_f32(w, kind, N, K)        -> binary32 weights before the bf16 rounding
 weights_f64(w, kind, N, K)       -> exact weights [N, K] (float64)
 matmul(w, kind, N, K, X, rows)   -> (Y, A): Y = X . W^T in binary64, A = sum |w x|
 repack_q4k(w, N, K)              -> q4_1 chunk bytes
+pack_q4_1(src, type, N, K)       -> q4_1 chunk bytes of a GGUF-type tensor ("From a GGUF")
+f16_to_f32(h)                    -> IEEE binary16 decoding
 argmax(logits)                   -> first maximum per row (NaN wins)
 
 Parity of the byte order inside a chunk is unpinned: no page prints it.
@@ -34,6 +36,8 @@ import threading
 import numpy as np
 
 Q4_1, Q4_K, Q8_KR, Q8_BLK = 1, 2, 3, 4
+SRC_Q4_0, SRC_Q4_1, SRC_Q8_0, SRC_F32, SRC_F16, SRC_BF16 = 1, 2, 3, 4, 5, 6
+SRC_BYTES_PER_32 = {SRC_Q4_0: 18, SRC_Q4_1: 20, SRC_Q8_0: 34, SRC_F32: 128, SRC_F16: 64, SRC_BF16: 64}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "q4nx_oracle.c")
@@ -77,6 +81,10 @@ def _load():
             lib.oracle_repack_q4k.restype = None
             lib.oracle_argmax.argtypes = [P, I64, I64, P]
             lib.oracle_argmax.restype = None
+            lib.oracle_pack_q4_1.argtypes = [P, I, I64, I64, P]
+            lib.oracle_pack_q4_1.restype = None
+            lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f32.restype = ctypes.c_float
             _lib = lib
     return _lib
 
@@ -177,3 +185,23 @@ def argmax(logits) -> np.ndarray:
     out = np.empty(L.shape[0], dtype=np.int32)
     _load().oracle_argmax(_ptr(L), L.shape[0], L.shape[1], _ptr(out))
     return out[0] if one_d else out
+
+
+def f16_to_f32(h) -> np.ndarray:
+    """IEEE binary16 bits -> binary32 values (exact)."""
+    h = np.asarray(h, dtype=np.uint16)
+    lib = _load()
+    return np.array([lib.oracle_f16_to_f32(int(v)) for v in h.reshape(-1)], dtype=np.float32).reshape(h.shape)
+
+
+def pack_q4_1(src, src_type: int, N: int, K: int) -> np.ndarray:
+    """q4_1 chunk bytes of the N x K tensor `src` (bytes) of GGUF type `src_type`."""
+    if N % 32 or K % 256 or N <= 0 or K <= 0:
+        raise ValueError(f"shape {N}x{K} is not a whole grid of 32x256 tiles")
+    src = np.ascontiguousarray(np.asarray(src).view(np.uint8).reshape(-1))
+    need = N * (K // 32) * SRC_BYTES_PER_32[src_type]
+    if src.size < need:
+        raise ValueError(f"{src.size} bytes given, {need} needed")
+    out = np.zeros((N // 32) * (K // 256) * 5120, dtype=np.uint8)
+    _load().oracle_pack_q4_1(_ptr(src), src_type, N, K, _ptr(out))
+    return out

@@ -290,3 +290,102 @@ void oracle_argmax(const float* logits, int64_t M, int64_t V, int32_t* idx)
         idx[m] = (int32_t)best;
     }
 }
+
+/* ------------------------------------------------------------------------
+ * GGUF-type tensors -> q4_1 chunks ("NPU engine" page, section "From a GGUF",
+ * the GGUF-type table):
+ *   Q4_0  -> scale d, zero -8d, codes unchanged   (error: bf16 rounding of scale and zero)
+ *   Q4_1  -> scale d, zero m,   codes unchanged   (same)
+ *   Q8_0, F32, F16, BF16 -> dequantized, then a min/max q4_1 per 32 columns (lossy)
+ *
+ * The page names the GGUF types but does not print their blocks.  Reading used
+ * (the GGUF block structs): a tensor [N][K] is row-major, a row is K/32 blocks
+ * of 32 consecutive columns;
+ *   Q4_0 block 18 B: fp16 d, 16 code bytes; element i < 16 is the low nibble of
+ *        byte i, element i >= 16 the high nibble of byte i - 16; value d*(q - 8)
+ *   Q4_1 block 20 B: fp16 d, fp16 m, 16 code bytes (as Q4_0); value d*q + m
+ *   Q8_0 block 34 B: fp16 d, 32 int8 codes; value d*q
+ *   F32 / F16 / BF16: N*K little-endian values.
+ * Min/max q4_1 of 32 values x (reading, made exact in binary32 one operation at
+ * a time): lo = min x, hi = max x; scale s = bf16((hi - lo) / 15); zero
+ * z = bf16(lo); code = clamp(rint((x - z) / s), 0, 15) with s, z the stored
+ * bf16 values (ties to even); every code is 0 when s == 0.  Inputs are finite.
+ */
+enum { ORC_SRC_Q4_0 = 1, ORC_SRC_Q4_1 = 2, ORC_SRC_Q8_0 = 3, ORC_SRC_F32 = 4, ORC_SRC_F16 = 5, ORC_SRC_BF16 = 6 };
+
+/* IEEE binary16 -> binary32 (exact): 1 sign, 5 exponent (bias 15), 10 fraction bits */
+float oracle_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 31, f = h & 1023;
+    float v;
+    if (e == 0) v = ldexpf((float)f, -24);                 /* zero and subnormals: f * 2^-24 */
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexpf((float)(f + 1024), e - 25);            /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+static void put16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
+
+/* value of element (n, k) of a dense or Q8_0 source, in binary32 */
+static float src_value(const uint8_t* src, int type, int64_t K, int64_t n, int64_t k)
+{
+    if (type == ORC_SRC_F32) { float v; memcpy(&v, src + (n * K + k) * 4, 4); return v; }
+    if (type == ORC_SRC_F16) return oracle_f16_to_f32(rd16(src + (n * K + k) * 2));
+    if (type == ORC_SRC_BF16) return oracle_bf16_to_f32(rd16(src + (n * K + k) * 2));
+    /* Q8_0 */
+    const uint8_t* blk = src + (n * (K / 32) + k / 32) * 34;
+    float d = oracle_f16_to_f32(rd16(blk));
+    int8_t q = (int8_t)blk[2 + k % 32];
+    return (float)q * d;                                    /* exact: 8 x 11 significant bits */
+}
+
+/* out: TR*TC q4_1 chunks of the N x K tensor `src` of GGUF type `type` */
+void oracle_pack_q4_1(const uint8_t* src, int type, int64_t N, int64_t K, uint8_t* out)
+{
+    int64_t TC = K / 256;
+    for (int64_t n = 0; n < N; ++n) {
+        int64_t tr = n / 32;
+        int r = (int)(n % 32);
+        for (int64_t b = 0; b < K / 32; ++b) {          /* one 32-column group of row n */
+            int64_t tc = b / 8;
+            int g = (int)(b % 8);
+            uint8_t* ch = out + (tr * TC + tc) * 5120;
+            int q[32];
+            uint16_t s_bits, z_bits;
+            if (type == ORC_SRC_Q4_0 || type == ORC_SRC_Q4_1) {
+                int bs = type == ORC_SRC_Q4_0 ? 18 : 20;
+                const uint8_t* blk = src + (n * (K / 32) + b) * bs;
+                float d = oracle_f16_to_f32(rd16(blk));
+                const uint8_t* qs = blk + (type == ORC_SRC_Q4_0 ? 2 : 4);
+                for (int i = 0; i < 32; ++i) q[i] = i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4);
+                s_bits = oracle_f32_to_bf16(d);
+                if (type == ORC_SRC_Q4_0) z_bits = oracle_f32_to_bf16(-8.0f * d);   /* exact product */
+                else z_bits = oracle_f32_to_bf16(oracle_f16_to_f32(rd16(blk + 2)));
+            } else {
+                float x[32], lo, hi;
+                for (int i = 0; i < 32; ++i) x[i] = src_value(src, type, K, n, b * 32 + i);
+                lo = hi = x[0];
+                for (int i = 1; i < 32; ++i) {
+                    if (x[i] < lo) lo = x[i];
+                    if (x[i] > hi) hi = x[i];
+                }
+                float range = hi - lo;
+                float step = range / 15.0f;
+                s_bits = oracle_f32_to_bf16(step);
+                z_bits = oracle_f32_to_bf16(lo);
+                float s = oracle_bf16_to_f32(s_bits), z = oracle_bf16_to_f32(z_bits);
+                for (int i = 0; i < 32; ++i) {
+                    if (s == 0.0f) { q[i] = 0; continue; }
+                    float t = x[i] - z;
+                    float u = t / s;
+                    float c = rintf(u);                     /* nearest, ties to even */
+                    q[i] = c < 0.0f ? 0 : (c > 15.0f ? 15 : (int)c);
+                }
+            }
+            for (int j = 0; j < 16; ++j)                    /* code (r, k) in byte r*128 + k/2, low nibble even k */
+                ch[r * 128 + g * 16 + j] = (uint8_t)(q[2 * j] | (q[2 * j + 1] << 4));
+            put16(ch + 4096 + (r * 8 + g) * 2, s_bits);
+            put16(ch + 4608 + (r * 8 + g) * 2, z_bits);
+        }
+    }
+}

@@ -203,3 +203,62 @@ def workload_activations(workload_id: int, matrix_id: int, M: int, K: int, layer
                          seed: int = 0) -> np.ndarray:
     """bf16 bits [M, K]; drawn from a stream separate from the weight's."""
     return activations(rng(workload_id, layer, 1000 + matrix_id, seed), M, K)
+
+
+# --------------------------------------------------------------------------
+# GGUF-type tensors (input of the q4_1 packer): blocks of 32 columns along a
+# row, row-major.  Q4_0: fp16 d + 16 code bytes (element i < 16 = low nibble
+# of byte i, i >= 16 = high nibble of byte i - 16); Q4_1: fp16 d, fp16 m + 16
+# code bytes; Q8_0: fp16 d + 32 int8 codes; dense: F32 / F16 / BF16 values.
+# --------------------------------------------------------------------------
+
+SRC_Q4_0, SRC_Q4_1, SRC_Q8_0, SRC_F32, SRC_F16, SRC_BF16 = 1, 2, 3, 4, 5, 6
+
+
+def _f16_bits(x: np.ndarray) -> np.ndarray:
+    return np.asarray(x, dtype=np.float16).view(np.uint16)
+
+
+def _gguf_nibbles(codes: np.ndarray) -> np.ndarray:
+    """[N, K/32, 32] codes 0..15 -> [N, K/32, 16] bytes (element i and i + 16 share byte i)."""
+    c = codes.astype(np.uint8)
+    return c[..., :16] | (c[..., 16:] << 4)
+
+
+def gguf_tensor(src_type: int, N: int, K: int, g: np.random.Generator) -> tuple[np.ndarray, dict]:
+    """Bytes of a synthetic N x K GGUF-type tensor and its logical fields.
+
+    Q4_0 / Q4_1: d = |N(0, 0.02)| / 8 (fp16), Q4_1 m = -8 d (1 + U(-0.1, 0.1)) (fp16), codes U{0..15};
+    Q8_0: d = |N(0, 0.005)| (fp16), codes U{-127..127}; dense: N(0, 0.02) values.
+    """
+    if N % 32 or K % 256:
+        raise ValueError("shape must be a whole grid of 32 x 256 tiles")
+    nb = K // 32
+    if src_type in (SRC_Q4_0, SRC_Q4_1):
+        d = np.abs(g.normal(0.0, 0.02, size=(N, nb))) / 8
+        codes = g.integers(0, 16, size=(N, nb, 32), dtype=np.int64)
+        dh = _f16_bits(d)
+        parts = [dh.reshape(N, nb, 1).view(np.uint8).reshape(N, nb, 2)]
+        f = {"d": dh, "codes": codes}
+        if src_type == SRC_Q4_1:
+            m = -8.0 * d * (1.0 + g.uniform(-0.1, 0.1, size=(N, nb)))
+            mh = _f16_bits(m)
+            parts.append(mh.reshape(N, nb, 1).view(np.uint8).reshape(N, nb, 2))
+            f["m"] = mh
+        parts.append(_gguf_nibbles(codes))
+        return np.concatenate(parts, axis=2).reshape(-1), f
+    if src_type == SRC_Q8_0:
+        d = _f16_bits(np.abs(g.normal(0.0, 0.005, size=(N, nb))))
+        codes = g.integers(-127, 128, size=(N, nb, 32), dtype=np.int8)
+        blk = np.concatenate([d.reshape(N, nb, 1).view(np.uint8).reshape(N, nb, 2), codes.view(np.uint8)], axis=2)
+        return blk.reshape(-1), {"d": d, "codes": codes}
+    x = g.normal(0.0, 0.02, size=(N, K))
+    if src_type == SRC_F32:
+        v = x.astype(np.float32)
+    elif src_type == SRC_F16:
+        v = x.astype(np.float16)
+    elif src_type == SRC_BF16:
+        v = bf16_bits(x)
+    else:
+        raise ValueError(f"unknown GGUF type {src_type}")
+    return np.ascontiguousarray(v).view(np.uint8).reshape(-1), {"values": v}
