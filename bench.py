@@ -472,6 +472,17 @@ def run_suite(args):
             emit({"suite": "gemv_top1", "workload": name, "M": 1, "us": us_f, "us_gemv_then_argmax": us_s,
                   "weight_gbs": nb / us_f / 1e3,
                   "roofline": {"bound": "hbm", "achieved": alg / us_f / 1e3, "peak": hbm, "frac": alg / us_f / 1e3 / hbm}})
+        if kind == synth.Q4_1 and wid == 4 and want("pack"):
+            # GGUF-type tensor of this shape -> q4_1 chunks (one-off conversion)
+            for st, sname in ((synth.SRC_Q4_0, "Q4_0"), (synth.SRC_Q4_1, "Q4_1"), (synth.SRC_F16, "F16")):
+                srcb, _ = synth.gguf_tensor(st, N, K, synth.rng(wid, 7, st))
+                srcs = [torch.from_numpy(srcb).to(dev) for _ in range(max(2, min(64, (512 << 20) // srcb.size + 1)))]
+                pout = torch.empty(nb, dtype=torch.uint8, device=dev)
+                us = timeit([lambda sb=sb: q.q4nx_pack_q4_1(sb, st, N, K, out=pout) for sb in srcs], 200)
+                alg = srcb.size + nb
+                emit({"suite": "pack_q4_1", "workload": f"{sname} {N}x{K} -> q4_1", "us": us,
+                      "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
+                del srcs
         if wid in (1, 5) and want("decode"):
             outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(min(R, 2))]
             us = timeit([lambda W=W, o=outs[i % len(outs)]: q.q4nx_decode(W, out=o) for i, W in enumerate(Ws)], 64)
@@ -523,7 +534,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
-    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,gemm_m64,argmax")
+    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_m64,argmax")
     ap.add_argument("--case", default="", help="suite: substring of the workload name")
     args = ap.parse_args()
     if args.warmup < 3:

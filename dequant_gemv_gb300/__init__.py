@@ -74,6 +74,7 @@ def _load():
         "q4nx_gemm_m64": ([W, P, I, P, I, P, U64, P], I),
         "q4nx_gemm_workspace": ([W, I], U64),
         "q4nx_repack_q4k": ([P, U64, I64, I64, P, U64, P], I),
+        "q4nx_pack_q4_1": ([I, P, U64, I64, I64, P, U64, P], I),
         "q4nx_argmax": ([P, I, I64, P, P], I),
         "q4nx_check": ([P, P], I),
         "q4nx_gemv_noalloc": ([W, P, P, I, P], I),
@@ -88,7 +89,7 @@ def _load():
 
 lib = _load()
 EXPORTS = ("q4nx_chunk_bytes", "q4nx_status_str", "q4nx_abi_version", "q4nx_decode", "q4nx_gemv",
-           "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_argmax",
+           "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_pack_q4_1", "q4nx_argmax",
            "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes")
 
 
@@ -289,6 +290,23 @@ def q4nx_gemm_m64(w: Weight, X: torch.Tensor, out: torch.Tensor | None = None, o
             ws = workspace(w.device, need)
         _check(lib.q4nx_gemm_m64(ctypes.byref(cw), X.data_ptr(), M, out.data_ptr(), code, ws.data_ptr(),
                                  ws.numel(), _stream(w.device)), "q4nx_gemm_m64")
+    return out
+
+
+Q4NX_SRC_Q4_0, Q4NX_SRC_Q4_1, Q4NX_SRC_Q8_0, Q4NX_SRC_F32, Q4NX_SRC_F16, Q4NX_SRC_BF16 = 1, 2, 3, 4, 5, 6
+
+
+def q4nx_pack_q4_1(src: torch.Tensor, src_type: int, rows: int, cols: int,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """q4_1 chunk bytes of a GGUF-type rows x cols tensor (`src`: its bytes, or a dense tensor)."""
+    _cuda(src, "src")
+    with torch.cuda.device(src.device):
+        if out is None:
+            out = torch.empty((rows // 32) * (cols // 256) * 5120, dtype=torch.uint8, device=src.device)
+        _cuda(out, "out")
+        _check(lib.q4nx_pack_q4_1(src_type, src.data_ptr(), src.numel() * src.element_size(), rows, cols,
+                                  out.data_ptr(), out.numel() * out.element_size(), _stream(src.device)),
+               "q4nx_pack_q4_1")
     return out
 
 

@@ -244,6 +244,20 @@ int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, i
                                out_dtype == Q4NX_OUT_F32, workspace_dev, static_cast<cudaStream_t>(stream)));
 }
 
+int q4nx_pack_q4_1(int src_type, const void* src_dev, uint64_t src_bytes, int64_t rows, int64_t cols, void* out_dev,
+                   uint64_t out_bytes, void* stream) {
+  if (src_dev == nullptr || out_dev == nullptr) return Q4NX_E_NULL;
+  const int bpb = pack_src_bytes_per_32(src_type);
+  if (bpb == 0) return Q4NX_E_KIND;
+  int st = check_grid(rows, cols);
+  if (st) return st;
+  const uint64_t T = static_cast<uint64_t>(rows / 32) * static_cast<uint64_t>(cols / 256);
+  if (src_bytes < static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols / 32) * bpb || out_bytes < T * kQ41Bytes)
+    return Q4NX_E_SHORT;
+  if (!aligned16(src_dev) || !aligned16(out_dev)) return Q4NX_E_ALIGN;
+  return from_cuda(launch_pack_q4_1(src_type, src_dev, rows / 32, cols / 256, out_dev, static_cast<cudaStream_t>(stream)));
+}
+
 int q4nx_repack_q4k(const void* in_dev, uint64_t in_bytes, int64_t rows, int64_t cols, void* out_dev,
                     uint64_t out_bytes, void* stream) {
   if (in_dev == nullptr || out_dev == nullptr) return Q4NX_E_NULL;

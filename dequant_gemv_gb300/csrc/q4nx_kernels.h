@@ -50,6 +50,11 @@ cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, 
 // ---- Q4_K -> q4_1 repack ----
 cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out, cudaStream_t s);
 
+// ---- GGUF-type tensor -> q4_1 chunks ----
+enum : int { kSrcQ4_0 = 1, kSrcQ4_1 = 2, kSrcQ8_0 = 3, kSrcF32 = 4, kSrcF16 = 5, kSrcBF16 = 6 };
+int pack_src_bytes_per_32(int src_type);        // 0 for an unknown type
+cudaError_t launch_pack_q4_1(int src_type, const void* src, int64_t TR, int64_t TC, void* out, cudaStream_t s);
+
 // ---- top-1 ----
 cudaError_t launch_argmax(const float* logits, int M, int64_t V, int32_t* idx, cudaStream_t s);
 

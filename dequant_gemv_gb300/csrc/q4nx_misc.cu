@@ -4,6 +4,7 @@
 // (chunk-kind table; the decoders-and-repack paragraph below it).  Greedy
 // top-1: the page's "Serving" section (greedy decoding).
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include "q4nx_device.cuh"
 #include "q4nx_kernels.h"
@@ -141,6 +142,151 @@ cudaError_t launch_repack_q4k(const void* in, int64_t TR, int64_t TC, void* out,
   if (T > 0x7FFFFFFF) return cudaErrorInvalidValue;
   repack_q4k_kernel<<<static_cast<unsigned>(T), 256, 0, s>>>(static_cast<const uint8_t*>(in),
                                                               static_cast<uint8_t*>(out));
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------- GGUF-type -> q4_1 ----
+//
+// "NPU engine" page, section "From a GGUF", GGUF-type table: Q4_0 becomes
+// scale d, zero -8d and Q4_1 scale d, zero m, codes unchanged (the only error
+// is the bf16 rounding of scale and zero); Q8_0, F32, F16 and BF16 are
+// dequantized, then quantized to a min/max q4_1 per 32 columns.  One CTA per
+// chunk, one thread per (row, 32-column group).  Source: row-major blocks of 32
+// columns (Q4_0: fp16 d + 16 code bytes, element i < 16 in the low nibble of
+// byte i and i >= 16 in the high nibble of byte i - 16; Q4_1: fp16 d, fp16 m +
+// the same 16 bytes; Q8_0: fp16 d + 32 int8), or N*K dense values.  Min/max
+// of 32 values x: lo, hi (first of equal minima / maxima); s = bf16((hi - lo)
+// / 15), z = bf16(lo); code = clamp(rint((x - z) / s), 0, 15) with the stored
+// s, z, ties to even, every code 0 if s == 0 -- each step one IEEE binary32
+// operation, so the codes are the same on every machine.
+
+__device__ __forceinline__ uint32_t ld_u16_global(const uint8_t* p) {
+  return *reinterpret_cast<const uint16_t*>(p);                   // 2-byte aligned by construction
+}
+
+template <int SRC>
+__global__ void __launch_bounds__(256) pack_q4_1_kernel(const uint8_t* __restrict__ src, int64_t K, int64_t TC,
+                                                        uint8_t* __restrict__ out) {
+  const int64_t t = blockIdx.x;
+  const int64_t tr = t / TC, tc = t - tr * TC;
+  const int r = threadIdx.x >> 3, g = threadIdx.x & 7;
+  const int64_t n = tr * 32 + r;                   // tensor row
+  const int64_t blk = n * (K / 32) + tc * 8 + g;   // 32-column block of that row
+  int q[32];
+  uint16_t s_bits, z_bits;
+  if constexpr (SRC == kSrcQ4_0 || SRC == kSrcQ4_1) {
+    constexpr int BS = SRC == kSrcQ4_0 ? 18 : 20;
+    const uint8_t* b = src + blk * BS;
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16_global(b))));
+    const uint8_t* qs = b + (SRC == kSrcQ4_0 ? 2 : 4);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t h = ld_u16_global(qs + 2 * j);   // bytes 2j, 2j+1
+      q[2 * j] = h & 15;
+      q[2 * j + 1] = (h >> 8) & 15;
+      q[16 + 2 * j] = (h >> 4) & 15;
+      q[16 + 2 * j + 1] = (h >> 12) & 15;
+    }
+    s_bits = f32_to_bf16_bits(d);
+    if constexpr (SRC == kSrcQ4_0) {
+      z_bits = f32_to_bf16_bits(__fmul_rn(-8.0f, d));                 // exact product
+    } else {
+      z_bits = f32_to_bf16_bits(__half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16_global(b + 2)))));
+    }
+  } else {
+    float x[32];
+    if constexpr (SRC == kSrcQ8_0) {
+      const uint8_t* b = src + blk * 34;
+      const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16_global(b))));
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t h = ld_u16_global(b + 2 + 2 * j);
+        x[2 * j] = __fmul_rn(static_cast<float>(static_cast<int8_t>(h & 0xFF)), d);     // exact
+        x[2 * j + 1] = __fmul_rn(static_cast<float>(static_cast<int8_t>(h >> 8)), d);
+      }
+    } else if constexpr (SRC == kSrcF32) {
+      const uint4* v = reinterpret_cast<const uint4*>(src + blk * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 u = v[j];
+        x[4 * j] = __uint_as_float(u.x);
+        x[4 * j + 1] = __uint_as_float(u.y);
+        x[4 * j + 2] = __uint_as_float(u.z);
+        x[4 * j + 3] = __uint_as_float(u.w);
+      }
+    } else {                                      // F16 or BF16: 32 values of 2 bytes
+      const uint4* v = reinterpret_cast<const uint4*>(src + blk * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 u = v[j];
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t h = hh ? (w4[e] >> 16) : (w4[e] & 0xFFFF);
+            x[8 * j + 2 * e + hh] = SRC == kSrcF16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+                                                  : bf16_bits_to_f32(h);
+          }
+        }
+      }
+    }
+    float lo = x[0], hi = x[0];
+#pragma unroll
+    for (int i = 1; i < 32; ++i) {
+      if (x[i] < lo) lo = x[i];
+      if (x[i] > hi) hi = x[i];
+    }
+    s_bits = f32_to_bf16_bits(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+    z_bits = f32_to_bf16_bits(lo);
+    const float sv = bf16_bits_to_f32(s_bits), zv = bf16_bits_to_f32(z_bits);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (sv == 0.0f) { q[i] = 0; continue; }
+      const float c = rintf(__fdiv_rn(__fsub_rn(x[i], zv), sv));      // nearest, ties to even
+      q[i] = c < 0.0f ? 0 : (c > 15.0f ? 15 : static_cast<int>(c));
+    }
+  }
+  uint8_t* ch = out + t * kQ41Bytes;
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w[j] = static_cast<uint32_t>(q[8 * j] | (q[8 * j + 1] << 4) | (q[8 * j + 2] << 8) | (q[8 * j + 3] << 12) |
+                                 (q[8 * j + 4] << 16) | (q[8 * j + 5] << 20) | (q[8 * j + 6] << 24) |
+                                 (q[8 * j + 7] << 28));
+  *reinterpret_cast<uint4*>(ch + r * 128 + g * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint16_t*>(ch + kQ41Scale)[r * 8 + g] = s_bits;
+  reinterpret_cast<uint16_t*>(ch + kQ41Zero)[r * 8 + g] = z_bits;
+}
+
+int pack_src_bytes_per_32(int src_type) {
+  switch (src_type) {
+    case kSrcQ4_0: return 18;
+    case kSrcQ4_1: return 20;
+    case kSrcQ8_0: return 34;
+    case kSrcF32: return 128;
+    case kSrcF16:
+    case kSrcBF16: return 64;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_pack_q4_1(int src_type, const void* src, int64_t TR, int64_t TC, void* out, cudaStream_t s) {
+  const int64_t T = TR * TC;
+  if (T > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const uint8_t* in = static_cast<const uint8_t*>(src);
+  uint8_t* o = static_cast<uint8_t*>(out);
+  const unsigned grid = static_cast<unsigned>(T);
+  const int64_t K = TC * 256;
+  switch (src_type) {
+    case kSrcQ4_0: pack_q4_1_kernel<kSrcQ4_0><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    case kSrcQ4_1: pack_q4_1_kernel<kSrcQ4_1><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    case kSrcQ8_0: pack_q4_1_kernel<kSrcQ8_0><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    case kSrcF32: pack_q4_1_kernel<kSrcF32><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    case kSrcF16: pack_q4_1_kernel<kSrcF16><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    case kSrcBF16: pack_q4_1_kernel<kSrcBF16><<<grid, 256, 0, s>>>(in, K, TC, o); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

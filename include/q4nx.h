@@ -160,6 +160,25 @@ uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M);
 int q4nx_repack_q4k(const void* in_dev, uint64_t in_bytes, int64_t rows, int64_t cols,
                     void* out_dev, uint64_t out_bytes, void* stream);
 
+/* GGUF-type tensor -> q4_1 chunks ("NPU engine" page, section "From a GGUF",
+ * GGUF-type table).  Q4NX_SRC_Q4_0 becomes scale d, zero -8d and Q4NX_SRC_Q4_1
+ * scale d, zero m, codes unchanged: the only error is the bf16 rounding of
+ * scale and zero.  Q4NX_SRC_Q8_0, _F32, _F16 and _BF16 are dequantized and
+ * quantized to a min/max q4_1 per 32 columns (lossy): lo, hi of the 32 values
+ * (the first of equal minima / maxima), scale = bf16((hi - lo) / 15),
+ * zero = bf16(lo), code = clamp(rint((x - zero) / scale), 0, 15) with the
+ * stored scale and zero (ties to even; 0 when scale is 0), each step one IEEE
+ * binary32 operation.  Inputs must be finite.
+ * src_dev: the rows x cols tensor, row-major, as GGUF blocks of 32 columns
+ * (Q4_0: 18 B = fp16 d + 16 code bytes, element i < 16 in the low nibble of
+ * byte i and i >= 16 in the high nibble of byte i - 16; Q4_1: 20 B = fp16 d,
+ * fp16 m + those 16 bytes; Q8_0: 34 B = fp16 d + 32 int8) or dense values
+ * (4 / 2 / 2 bytes each); 16-byte aligned; at least rows * cols/32 blocks.
+ * out_dev: (rows/32)*(cols/256)*5120 bytes, 16-byte aligned. */
+enum { Q4NX_SRC_Q4_0 = 1, Q4NX_SRC_Q4_1 = 2, Q4NX_SRC_Q8_0 = 3, Q4NX_SRC_F32 = 4, Q4NX_SRC_F16 = 5, Q4NX_SRC_BF16 = 6 };
+int q4nx_pack_q4_1(int src_type, const void* src_dev, uint64_t src_bytes, int64_t rows, int64_t cols, void* out_dev,
+                   uint64_t out_bytes, void* stream);
+
 /* Top-1 of each row of fp32 logits [M][V] (greedy decoding, "Serving" section):
  * idx_dev[m] = index of the first maximum; a NaN counts above every number and
  * the first NaN wins; +0 and -0 are equal.  1 <= M <= 65535, 1 <= V < 2^31. */

@@ -80,6 +80,13 @@ def test_validation_statuses(q):
     assert L.q4nx_gemv(by(w), P, P, 0, None, need, None) == 7
     assert L.q4nx_gemv(by(w), P, P, 0, P, need - 1, None) == 7
     assert L.q4nx_gemv(by(w), P + 2, P, 0, P, need, None) == 5
+    # GGUF-type pack: unknown source type, shape, short buffers, alignment
+    assert L.q4nx_pack_q4_1(9, P, 1 << 30, 32, 256, P, 5120, None) == 2
+    assert L.q4nx_pack_q4_1(1, P, 1 << 30, 31, 256, P, 5120, None) == 3
+    assert L.q4nx_pack_q4_1(1, P, 32 * 8 * 18 - 1, 32, 256, P, 5120, None) == 4
+    assert L.q4nx_pack_q4_1(1, P, 32 * 8 * 18, 32, 256, P, 5119, None) == 4
+    assert L.q4nx_pack_q4_1(1, P + 2, 1 << 20, 32, 256, P, 5120, None) == 5
+    assert L.q4nx_pack_q4_1(1, None, 1 << 20, 32, 256, P, 5120, None) == 1
     # fused top-1: same weight checks; the index pointer needs 4-byte alignment
     assert L.q4nx_gemv_top1(by(w), P, None, P, need, None) == 1
     assert L.q4nx_gemv_top1(by(w), P, P + 2, P, need, None) == 5
