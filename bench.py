@@ -260,7 +260,14 @@ def run_gpu(args, rank: int, world: int):
             fn()
         return g
 
-    graph = capture(step_batch)
+    graph = capture(step_batch)                 # one step (used for the end-to-end leg)
+    # the timed loop replays graphs of several consecutive steps, so that each
+    # step's launch overlaps the previous one (programmatic dependent launch)
+    # as in a decode loop; a step is still one launch over all 196 matrices
+    per_graph = max(1, min(8, args.steps))
+    graph_many = capture(lambda: [step_batch() for _ in range(per_graph)])
+    rem = args.steps % per_graph
+    graph_rem = capture(lambda: [step_batch() for _ in range(rem)]) if rem else None
     launches_per_step = 1
 
     def barrier():
@@ -271,6 +278,7 @@ def run_gpu(args, rank: int, world: int):
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
+        graph_many.replay()
     stream.synchronize()
 
     gpu_uuid = None
@@ -287,8 +295,10 @@ def run_gpu(args, rank: int, world: int):
     time.sleep(0.3)                              # let the sampler start before the timed region
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        for _ in range(args.steps // per_graph):
+            graph_many.replay()
+        if graph_rem is not None:
+            graph_rem.replay()
         ev1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -359,7 +369,8 @@ def run_gpu(args, rank: int, world: int):
             "config": {"workload": WORKLOAD, "layers": synth.QWEN3_06B_LAYERS, "matrices_per_step": len(mats),
                        "weight_bytes_per_step": wtot, "kind": "q4_1", "batch": 1,
                        "l2": "inputs larger than L2 (275 MB of weights streamed per step)",
-                       "launch": "one q4nx_gemv_batch launch of all 196 matrices per step, CUDA-graph replay",
+                       "launch": "one q4nx_gemv_batch launch of all 196 matrices per step; CUDA graphs of "
+                                 f"{per_graph} consecutive steps, replayed back to back",
                        "other_schedules": alt,
                        "hbm_frac_of_nominal_8tbs": value / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -496,6 +507,18 @@ def run_suite(args):
             alg = nb + rep.numel()
             emit({"suite": "repack", "workload": name, "us": us,
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
+        if kind == synth.Q4_1 and wid == 4 and want("gemm_small_m"):
+            # small token blocks (verify windows, multi-token prediction) through the same GEMM
+            for M in (2, 4, 8, 16):
+                X = dev_bf16(synth.workload_activations(wid, 0, M, K))
+                Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                with torch.cuda.stream(stream):
+                    gws = torch.zeros(int(q.lib.q4nx_gemm_workspace(ctypes.byref(Ws[0].c()), M)), dtype=torch.uint8,
+                                      device=dev)
+                us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, ws=gws) for W in Ws], 400)
+                alg = nb + 2 * M * K + 2 * M * N
+                emit({"suite": "gemm_small_m", "workload": name, "M": M, "us": us, "weight_gbs": nb / us / 1e3,
+                      "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
         if ((kind == synth.Q4_1 and wid == 4) or wid == 5) and want("gemm_m64"):
             M = 64
             X = dev_bf16(synth.workload_activations(wid, 0, M, K))
@@ -534,7 +557,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
-    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_m64,argmax")
+    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_small_m,gemm_m64,argmax")
     ap.add_argument("--case", default="", help="suite: substring of the workload name")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -298,7 +298,7 @@ cudaError_t launch_pack_q4_1(int src_type, const void* src, int64_t TR, int64_t 
 // CTA scans an eighth, then CTA 0 reads the others' maxima through
 // distributed shared memory.  No workspace, no atomics, deterministic.
 constexpr int kArgmaxCluster = 8;
-constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxThreads = 512;
 
 
 __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
@@ -317,7 +317,23 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
   if (vec && b1 > b0) {
     const int64_t n4 = (b1 - b0) / 4;
     const float4* r4 = reinterpret_cast<const float4*>(row + b0);
-    for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    // four loads in flight per thread before any is used: the scan is
+    // latency-bound, not bandwidth-bound, at one row of ~150K logits
+    int64_t i = threadIdx.x;
+    for (; i + 3 * kArgmaxThreads < n4; i += 4 * kArgmaxThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(r4 + i + u * kArgmaxThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t k = static_cast<uint32_t>(b0 + 4 * (i + u * kArgmaxThreads));
+        best = umax64(best, argmax_key(v[u].x, k));
+        best = umax64(best, argmax_key(v[u].y, k + 1));
+        best = umax64(best, argmax_key(v[u].z, k + 2));
+        best = umax64(best, argmax_key(v[u].w, k + 3));
+      }
+    }
+    for (; i < n4; i += kArgmaxThreads) {
       const float4 v = __ldg(r4 + i);
       const uint32_t k = static_cast<uint32_t>(b0 + 4 * i);
       best = umax64(best, argmax_key(v.x, k));

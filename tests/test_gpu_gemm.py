@@ -129,3 +129,13 @@ def test_gemm_q8_layouts_agree_on_the_same_weights(q):
     a = q.q4nx_gemm_m64(q.Weight(to_dev_bytes(wkr), synth.Q8_KR, N, K), X, out_dtype="f32")
     b = q.q4nx_gemm_m64(q.Weight(to_dev_bytes(wblk), synth.Q8_BLK, N, K), X, out_dtype="f32")
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+# ---- small token blocks (verify windows, multi-token prediction blocks): M in {2, 4, 8, 16} ----
+
+@pytest.mark.parametrize("M", [2, 4, 8, 16])
+@pytest.mark.parametrize("kind,N,K,wid", [(synth.Q4_1, 4096, 4096, 4), (synth.Q8_BLK, 2048, 2560, 5)])
+def test_gemm_small_token_blocks(q, M, kind, N, K, wid):
+    rows = np.unique(np.concatenate([np.arange(0, 128), np.arange(N - 128, N),
+                                     np.random.default_rng(M).integers(0, N, 300)]))
+    run(q, kind, N, K, M, out="bf16" if kind == synth.Q4_1 else "f32", rows=rows, wid=wid)
