@@ -141,14 +141,20 @@ def _cuda(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
-# Workspaces: zero-filled once, left zero-filled by every call (see q4nx.h).
-# One per (device, stream); calls on one stream are ordered, so they never overlap.
+# Workspaces: zero-filled once.  The GEMV family (q4nx_gemv, _gemv_top1,
+# _gemv_batch) leaves its workspace zero-filled after every call and relies on
+# that; the GEMM leaves partial tiles behind, so the two families never share
+# one.  One per (family, device, stream); calls on one stream are ordered, so
+# they never overlap.
 _ws_lock = threading.Lock()
-_ws: dict[tuple[int, int], torch.Tensor] = {}
+_ws: dict[tuple[str, int, int], torch.Tensor] = {}
+WS_FAMILIES = ("gemv", "gemm")
 
 
-def workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    key = (device.index if device.index is not None else torch.cuda.current_device(), _stream(device))
+def workspace(device: torch.device, nbytes: int, family: str = "gemv") -> torch.Tensor:
+    if family not in WS_FAMILIES:
+        raise ValueError(f"unknown workspace family {family!r}")
+    key = (family, device.index if device.index is not None else torch.cuda.current_device(), _stream(device))
     with _ws_lock:
         t = _ws.get(key)
         if t is None or t.numel() < nbytes:
@@ -287,7 +293,7 @@ def q4nx_gemm_m64(w: Weight, X: torch.Tensor, out: torch.Tensor | None = None, o
         cw = w.c()
         need = int(lib.q4nx_gemm_workspace(ctypes.byref(cw), M))
         if ws is None:
-            ws = workspace(w.device, need)
+            ws = workspace(w.device, need, "gemm")
         _check(lib.q4nx_gemm_m64(ctypes.byref(cw), X.data_ptr(), M, out.data_ptr(), code, ws.data_ptr(),
                                  ws.numel(), _stream(w.device)), "q4nx_gemm_m64")
     return out
@@ -336,8 +342,12 @@ def q4nx_argmax(logits: torch.Tensor, out: torch.Tensor | None = None) -> torch.
 
 
 def q4nx_check(ws: torch.Tensor | None = None, device=None) -> None:
-    """Raise if a bounded in-kernel wait of an earlier call on this workspace gave up."""
-    if ws is None:
-        device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-        ws = workspace(device, 16)
-    _check(lib.q4nx_check(ws.data_ptr(), _stream(ws.device)), "q4nx_check")
+    """Raise if a bounded in-kernel wait of an earlier call on this workspace (default:
+    this stream's GEMV and GEMM workspaces) gave up."""
+    if ws is not None:
+        _check(lib.q4nx_check(ws.data_ptr(), _stream(ws.device)), "q4nx_check")
+        return
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    for family in WS_FAMILIES:
+        w = workspace(device, 16, family)
+        _check(lib.q4nx_check(w.data_ptr(), _stream(w.device)), "q4nx_check")

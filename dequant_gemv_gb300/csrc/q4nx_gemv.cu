@@ -49,7 +49,6 @@ struct GemvItemDev {
   int64_t cbase;           // first chunk of this item in the batch index space
   int64_t nchunks;         // TR * TC
   int32_t TC;
-  int32_t trbase;          // first tile row of this item in the batch's counter array
 };
 
 // Kernel parameters; MAXB batch slots (instantiated for 1, 8 and 256 items so
@@ -63,8 +62,7 @@ struct GemvArgsT {
   int out_f32;
   int64_t T;               // chunks in the batch
   uint32_t* err;
-  uint32_t* counters;      // [sum TR]
-  float* partials;         // [grid][2][32]: a CTA's first and last tile row when other CTAs share them
+  uint64_t* posted;        // [grid][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
   // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
   // row) key; the last CTA to finish writes the row index
   int32_t* top1_idx;       // null: store y
@@ -119,45 +117,42 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
 // A tile row [r0, r1) shared with other CTAs, after this CTA's warps have
 // combined their parts (lane = row, `val` = this CTA's sum).  The CTA holding
 // the row's first chunk finishes it: it reaches its part last (at the end of
-// its range), so the others have usually posted theirs long before.  The
-// others post their sum in their slot 0 and count themselves in with a
-// release reduction; the finisher waits (bounded) for the count, adds the
-// posted sums in CTA order after its own, stores y and clears what it used.
+// its range), so the others have usually posted theirs long before.  A
+// poster writes, per row, one 64-bit word holding its sum and a ready flag,
+// so the value and its readiness travel together and one read serves both;
+// the finisher reads the posted words (waiting, bounded, for any not yet
+// ready), adds them in CTA order after its own sum, stores y and clears the
+// words it used.
+constexpr uint64_t kPosted = 1ull << 32;
+
 template <class GemvArgs>
 __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t Lc, int it, int64_t tr, int64_t r0,
                                            int64_t r1, float val, int lane) {
   const GemvItemDev& item = a.items[it];
-  uint32_t* counter = &a.counters[item.trbase + tr];
   if (r0 < Lc) {                                      // not the finisher: post
-    a.partials[(b * 2) * 32 + lane] = val;
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) red_release_add(counter, 1u);
+    st_relaxed_u64(&a.posted[b * 32 + lane], kPosted | __float_as_uint(val));
     return;
   }
   const int64_t c_last = cta_of(r1 - 1, a.T, a.grid);
-  const uint32_t expect = static_cast<uint32_t>(c_last - b);
-  uint32_t ok = 1;
-  if (lane == 0) {
-    if (ld_acquire_u32(counter) != expect) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u32(counter) != expect) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) { ok = 0; atomicOr(a.err, 1u); break; }
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) return;
-  __syncwarp();
   float sum = val;
   for (int64_t c = b + 1; c <= c_last; ++c) {
-    float* p = &a.partials[(c * 2) * 32 + lane];
-    sum += ld_cg_f32(p);
-    *p = 0.f;                                       // leave the workspace zero-filled
+    uint64_t* p = &a.posted[c * 32 + lane];
+    uint64_t w = ld_relaxed_u64(p);
+    if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
+      const uint64_t t0 = globaltimer_ns();
+      while ((w & kPosted) == 0) {
+        w = ld_relaxed_u64(p);
+        if ((w & kPosted) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+      }
+      if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
+        if (lane == 0) atomicOr(a.err, 1u);
+        return;
+      }
+    }
+    sum += __uint_as_float(static_cast<uint32_t>(w));
+    *p = 0ull;                                        // leave the workspace zero-filled
   }
   store_y(a, item.y, tr * 32 + lane, sum);
-  __syncwarp();
-  if (lane == 0) *counter = 0u;
 }
 
 // ------------------------------------------------------- chunk bodies ----
@@ -184,14 +179,44 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+// A q4 chunk's share of one lane, read out of the ring stage at once so that
+// the stage can be refilled before the arithmetic starts.  Prep lane
+// (gp = lane & 7, tp = lane >> 3) reads the 8 columns gp*32 + 8tp .. +7 of
+// the x slice (code word tp of group gp); decode lane (qr = lane >> 3,
+// g = lane & 7) reads rows 4i + qr of group g: 16 code bytes and the
+// group's scale fields per row.
 template <int KIND>
-__device__ __forceinline__ void q4_chunk(uint32_t st, uint32_t scratch, int lane, float (&yacc)[8]) {
+struct Q4Lane {
+  uint4 xr;
+  uint4 cw[8];
+  uint32_t f0[8], f1[8];           // q4_1: scale, zero bits; Q4_K: S bits | M bits << 16, sc | mn << 16
+};
+
+template <int KIND>
+__device__ __forceinline__ void q4_read(uint32_t st, int lane, Q4Lane<KIND>& L) {
   constexpr int CB = chunk_bytes_of(KIND);
-  // ---- x slice -> byte planes.  Prep lane (gp = lane & 7, tp = lane >> 3) owns the
-  // 8 columns gp*32 + 8tp .. +7 of the slice, i.e. code word tp of group gp.
   const int gp = lane & 7, tp = lane >> 3;
-  const uint4 xr = lds128(st + CB + gp * 64 + tp * 16);
-  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+  L.xr = lds128(st + CB + gp * 64 + tp * 16);
+  const int qr = lane >> 3, g = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + qr;
+    L.cw[i] = lds128(st + r * 128 + g * 16);
+    if constexpr (KIND == kQ4_1) {
+      L.f0[i] = lds_u16(st + kQ41Scale + (r * 8 + g) * 2);
+      L.f1[i] = lds_u16(st + kQ41Zero + (r * 8 + g) * 2);
+    } else {
+      L.f0[i] = lds_u16(st + kQ4KS + r * 2) | (lds_u16(st + kQ4KM + r * 2) << 16);
+      L.f1[i] = lds_u8(st + kQ4KSc + r * 8 + g) | (lds_u8(st + kQ4KMn + r * 8 + g) << 16);
+    }
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void q4_compute(const Q4Lane<KIND>& L, uint32_t scratch, int lane, float (&yacc)[8]) {
+  // ---- x slice -> byte planes
+  const int gp = lane & 7, tp = lane >> 3;
+  const uint32_t xw[4] = {L.xr.x, L.xr.y, L.xr.z, L.xr.w};
   uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
                          __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
   uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
@@ -220,27 +245,23 @@ __device__ __forceinline__ void q4_chunk(uint32_t st, uint32_t scratch, int lane
                "r"(p1e), "r"(p1o)
                : "memory");
   __syncwarp();
-  // ---- decode lane (q = lane >> 3, g = lane & 7): rows 4i + q of group g
-  const int qr = lane >> 3, g = lane & 7;
+  // ---- decode lane: rows 4i + qr of group g
+  const int g = lane & 7;
   uint4 P[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) P[t] = lds128(scratch + (t * 8 + g) * 16);
   __syncwarp();                                                 // scratch is rewritten by the next chunk
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + qr;
-    const uint4 cw = lds128(st + r * 128 + g * 16);
     float s, z;
     if constexpr (KIND == kQ4_1) {
-      s = bf16_bits_to_f32(lds_u16(st + kQ41Scale + (r * 8 + g) * 2));
-      z = bf16_bits_to_f32(lds_u16(st + kQ41Zero + (r * 8 + g) * 2));
+      s = bf16_bits_to_f32(L.f0[i]);
+      z = bf16_bits_to_f32(L.f1[i]);
     } else {
-      const float S = bf16_bits_to_f32(lds_u16(st + kQ4KS + r * 2));
-      const float M = bf16_bits_to_f32(lds_u16(st + kQ4KM + r * 2));
-      s = S * static_cast<float>(lds_u8(st + kQ4KSc + r * 8 + g));
-      z = M * static_cast<float>(lds_u8(st + kQ4KMn + r * 8 + g));
+      s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * static_cast<float>(L.f1[i] & 0xFFFFu);
+      z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
     }
-    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t w[4] = {L.cw[i].x, L.cw[i].y, L.cw[i].z, L.cw[i].w};
     uint32_t s0 = 0;
     int s1 = 0;
 #pragma unroll
@@ -469,7 +490,10 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
       seg_tr = cur.tr;
     }
     const uint32_t st = smem_u32(ring + s * SB);
-    if constexpr (Q4) q4_chunk<KIND>(st, scratch, lane, yacc);
+    // 4-bit chunks: the lanes take their share of the stage into registers
+    // and the stage is refilled before the arithmetic; Q8: after it
+    Q4Lane<Q4 ? KIND : kQ4_1> q4l;
+    if constexpr (Q4) q4_read<KIND>(st, lane, q4l);
     else q8_chunk<KIND>(st, lane, yacc);
     __syncwarp();
     if (lane == 0 && j + stages < n) {
@@ -477,6 +501,7 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
       issue_xslice<KIND>(a, pre, ring + s * SB, &bars[s]);
       pre.next(a);
     }
+    if constexpr (Q4) q4_compute<KIND>(q4l, scratch, lane, yacc);
     cur.next(a);
     if (++s == stages) s = 0;
   }
@@ -551,7 +576,8 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
 
 uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks) {
   (void)total_chunks;
-  return kWsErrBytes + align16(static_cast<uint64_t>(total_tile_rows) * 4) + static_cast<uint64_t>(kMaxCtas) * 2 * 32 * 4;
+  (void)total_tile_rows;
+  return kWsErrBytes + static_cast<uint64_t>(kMaxCtas) * 32 * 8;
 }
 
 template <int KIND, int MAXB>
@@ -581,7 +607,7 @@ template <int MAXB>
 static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                                      const DeviceInfo& info, int32_t* top1_idx, cudaStream_t s) {
   GemvArgsT<MAXB> a;
-  int64_t T = 0, TRsum = 0;
+  int64_t T = 0;
   for (int i = 0; i < n; ++i) {
     a.items[i].chunks = static_cast<const uint8_t*>(items[i].chunks);
     a.items[i].x = static_cast<const uint8_t*>(items[i].x);
@@ -589,9 +615,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
     a.items[i].cbase = T;
     a.items[i].nchunks = items[i].TR * items[i].TC;
     a.items[i].TC = static_cast<int32_t>(items[i].TC);
-    a.items[i].trbase = static_cast<int32_t>(TRsum);
     T += items[i].TR * items[i].TC;
-    TRsum += items[i].TR;
   }
   GemvPlan p;
   if (!gemv_plan(kind, T, info, &p)) return cudaErrorInvalidValue;
@@ -605,8 +629,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   a.top1_idx = top1_idx;
   a.top1_done = reinterpret_cast<uint32_t*>(ws + 4);
   a.top1_key = reinterpret_cast<uint64_t*>(ws + 8);
-  a.counters = reinterpret_cast<uint32_t*>(ws + kWsErrBytes);
-  a.partials = reinterpret_cast<float*>(ws + kWsErrBytes + align16(static_cast<uint64_t>(TRsum) * 4));
+  a.posted = reinterpret_cast<uint64_t*>(ws + kWsErrBytes);
   switch (kind) {
     case kQ4_1: return launch_gemv_t<kQ4_1, MAXB>(a, p, s);
     case kQ4_K: return launch_gemv_t<kQ4_K, MAXB>(a, p, s);

@@ -1,8 +1,8 @@
 // q4nx_noalloc.cu -- q4nx_gemv_noalloc: the fused decode + GEMV with its scratch
 // memory built into the library, for callers that cannot allocate device memory.
 //
-// The GEMV needs scratch (an error word, one arrival counter per tile row and
-// the partial sums of tile rows shared between CTAs).  q4nx_gemv takes it from
+// The GEMV needs scratch (an error word and the posted partial sums of tile
+// rows shared between CTAs, 16 B + 256 KiB whatever the weight's size).  q4nx_gemv takes it from
 // the caller; this entry point instead uses kNoAllocScratchBytes of statically
 // allocated device memory that every GPU loading the library holds until the
 // process exits.  Host code never dereferences the array's name: the device
@@ -64,17 +64,16 @@ int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int 
     return Q4NX_E_ALIGN;
   if (out_dtype != Q4NX_OUT_BF16 && out_dtype != Q4NX_OUT_F32) return Q4NX_E_DTYPE;
   const uint64_t need = gemv_workspace_bytes(TR, TR * TC);
-  if (need > kNoAllocScratchBytes) return Q4NX_E_WORKSPACE;          // more tile rows than the built-in scratch holds
+  if (need > kNoAllocScratchBytes) return Q4NX_E_WORKSPACE;          // cannot happen: the need is a constant
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return Q4NX_E_CUDA;
   DeviceInfo info;
   if (device_info(&info) != cudaSuccess) return Q4NX_E_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The error word and the arrival counters must start at zero; the array keeps
-  // whatever the previous call left, so clear them (the partial sums are
-  // always written before they are read).
-  if (cudaMemsetAsync(scratch, 0, kWsErrBytes + align16(static_cast<uint64_t>(TR) * 4), s) != cudaSuccess)
-    return Q4NX_E_CUDA;
+  // The error word and the posted words (value + ready flag) must start at
+  // zero; the array keeps whatever the previous call left, an abandoned call
+  // included, so clear them.
+  if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return Q4NX_E_CUDA;
   GemvItem item;
   item.chunks = w->chunks_dev;
   item.x = x_dev;

@@ -101,7 +101,8 @@ int q4nx_decode(const q4nx_weight* w, void* out_dev, uint64_t out_bytes, void* s
  * workspace_dev: device scratch of at least q4nx_gemv_workspace(w) bytes, 16-byte
  * aligned, ZERO-FILLED before its first use; every call leaves it zero-filled
  * again (after Q4NX_E_DEVICE_TIMEOUT it must be zero-filled anew).  It holds
- * split-K partial sums, per-tile-row arrival counters and an error word.
+ * an error word and the partial sums of tile rows split between CTAs, each
+ * posted with a ready flag (16 B + 256 KiB for any weight).
  * Results are deterministic: partials are added in a fixed order. */
 int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype,
               void* workspace_dev, uint64_t workspace_bytes, void* stream);
@@ -189,19 +190,19 @@ int q4nx_argmax(const float* logits_dev, int M, int64_t V, int32_t* idx_dev, voi
  * example a real-time decode loop, or a plug-in inside a framework that owns
  * every device allocation and hands out only inputs and outputs).  The pages
  * have no counterpart of this entry point; it is q4nx_gemv with its scratch
- * memory (error word, per-tile-row counters, partial sums) taken from a 1 MiB
+ * memory (error word, posted partial sums) taken from a 1 MiB
  * array compiled into the library, which every GPU that loads the library
  * keeps until the process exits.
  * The caller passes inputs and outputs only, exactly as for q4nx_gemv.
  * The first call on each device looks up that device's copy of the array
  * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call clears the counters it uses, so a call never depends on what an
+ * Every call clears the scratch it uses, so a call never depends on what an
  * earlier call left behind; but all calls on a device share the one array, so
  * calls that can overlap on the GPU (different streams, or concurrent graph
  * branches) race and must be serialised by the caller.
- * Returns Q4NX_E_WORKSPACE if the weight needs more scratch than the array
- * holds (q4nx_noalloc_scratch_bytes(); tile rows beyond about 196 000);
- * otherwise the statuses of q4nx_gemv.  Calls no cudaMalloc or cudaFree. */
+ * The scratch a call needs does not grow with the weight, so every weight that
+ * q4nx_gemv accepts fits q4nx_noalloc_scratch_bytes(); the statuses are those
+ * of q4nx_gemv.  Calls no cudaMalloc or cudaFree. */
 int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype, void* stream);
 uint64_t q4nx_noalloc_scratch_bytes(void);
 

@@ -71,11 +71,12 @@ def test_noalloc_matches_workspace_entry_point(q, kind, N, K, out):
         assert np.all(np.abs(got[rows] - ref[rows]) <= tol), f"call {call}"
 
 
-def test_noalloc_rejects_more_tile_rows_than_its_scratch(q):
+def test_noalloc_scratch_covers_any_weight(q):
+    # host-side sizes only: the scratch a GEMV needs does not grow with the
+    # weight, so the built-in array serves every shape q4nx_gemv accepts
     cap = int(q.lib.q4nx_noalloc_scratch_bytes())
     assert cap == 1 << 20
-    t = torch.zeros(16, dtype=torch.uint8, device=DEV)
-    rows = 32 * 300000                               # 300 000 tile rows: more than 1 MiB of counters
-    cw = q.q4nx_weight(t.data_ptr(), 1 << 62, synth.Q4_1, 0, rows, 256)
-    st = q.lib.q4nx_gemv_noalloc(ctypes.byref(cw), t.data_ptr(), t.data_ptr(), 0, None)
-    assert st == 7, q.q4nx_status_str(st)           # Q4NX_E_WORKSPACE, nothing launched
+    for rows, cols in [(32, 256), (151936, 2560), (32 * 300000, 256), (32 * 4096, 256 * 4096)]:
+        cw = q.q4nx_weight(0x1000, 1 << 62, synth.Q4_1, 0, rows, cols)
+        need = int(q.lib.q4nx_gemv_workspace(ctypes.byref(cw)))
+        assert 0 < need <= cap, (rows, cols, need)
