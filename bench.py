@@ -507,17 +507,21 @@ def run_suite(args):
             alg = nb + rep.numel()
             emit({"suite": "repack", "workload": name, "us": us,
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
-        if kind == synth.Q4_1 and wid == 4 and want("gemm_small_m"):
-            # small token blocks (verify windows, multi-token prediction) through the same GEMM
-            for M in (2, 4, 8, 16):
+        small_ms = {synth.Q4_1: (2, 3, 4, 8, 16), synth.Q4_K: (2, 4), synth.Q8_KR: (2, 4), synth.Q8_BLK: (2,)}
+        if ((kind == synth.Q4_1 and wid == 4) or kind == synth.Q4_K or wid == 5) and want("gemm_small_m"):
+            # small token blocks (verify windows, multi-token prediction): two tokens (Q4_K: up
+            # to four) on the CUDA cores, more on the tensor cores
+            for M in small_ms[kind]:
                 X = dev_bf16(synth.workload_activations(wid, 0, M, K))
-                Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                Y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
                 with torch.cuda.stream(stream):
                     gws = torch.zeros(int(q.lib.q4nx_gemm_workspace(ctypes.byref(Ws[0].c()), M)), dtype=torch.uint8,
                                       device=dev)
-                us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, ws=gws) for W in Ws], 400)
-                alg = nb + 2 * M * K + 2 * M * N
-                emit({"suite": "gemm_small_m", "workload": name, "M": M, "us": us, "weight_gbs": nb / us / 1e3,
+                us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, out_dtype=od, ws=gws) for W in Ws], 400)
+                alg = nb + 2 * M * K + (4 if out_f32 else 2) * M * N
+                cores = "cuda" if M <= (4 if kind == synth.Q4_K else 2) else "tensor"
+                emit({"suite": "gemm_small_m", "workload": name, "M": M, "path": cores, "us": us,
+                      "weight_gbs": nb / us / 1e3,
                       "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
         if ((kind == synth.Q4_1 and wid == 4) or wid == 5) and want("gemm_m64"):
             M = 64

@@ -223,9 +223,17 @@ int q4nx_gemv_top1(const q4nx_weight* w, const void* x_dev, int32_t* idx_dev, vo
   return from_cuda(launch_gemv_top1(w->kind, item, idx_dev, workspace_dev, info, static_cast<cudaStream_t>(stream)));
 }
 
+// Workspace of q4nx_gemm_m64: the GEMM's part (error word, posting counters,
+// partial tiles; partial tiles stay behind after a call) followed by the
+// few-token GEMV's part (posted row sums, left zero-filled).  Both share the
+// error word at offset 0, and one size serves every M.
+static uint64_t gemm_part_bytes(const q4nx_weight* w) {
+  return align16(gemm_workspace_bytes(w->rows / 32, w->cols / 256, 64));
+}
+
 uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M) {
   if (w == nullptr || check_grid(w->rows, w->cols) != Q4NX_OK || M < 1 || M > 64) return 0;
-  return gemm_workspace_bytes(w->rows / 32, w->cols / 256, M);
+  return gemm_part_bytes(w) + gemv_workspace_bytes(w->rows / 32, (w->rows / 32) * (w->cols / 256), kGemvTokensMax);
 }
 
 int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, int out_dtype, void* workspace_dev,
@@ -236,12 +244,28 @@ int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, i
   if (M < 1 || M > 64) return Q4NX_E_M;
   if (out_dtype != Q4NX_OUT_BF16 && out_dtype != Q4NX_OUT_F32) return Q4NX_E_DTYPE;
   if (!aligned16(X_dev) || !aligned16(Y_dev)) return Q4NX_E_ALIGN;
-  if (!gemm_supports(w->kind)) return Q4NX_E_UNSUPPORTED;
-  if (workspace_dev == nullptr || workspace_bytes < gemm_workspace_bytes(w->rows / 32, w->cols / 256, M))
-    return Q4NX_E_WORKSPACE;
+  const bool tokens = M <= gemv_max_tokens(w->kind);
+  if (!tokens && !gemm_supports(w->kind)) return Q4NX_E_UNSUPPORTED;
+  if (workspace_dev == nullptr || workspace_bytes < q4nx_gemm_workspace(w, M)) return Q4NX_E_WORKSPACE;
   if (!aligned16(workspace_dev)) return Q4NX_E_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tokens) {
+    // a few tokens: each chunk is decoded once for all of them on the CUDA
+    // cores, cheaper than the tensor-core path's decode of every weight to bf16
+    DeviceInfo info;
+    if (device_info(&info) != cudaSuccess) return Q4NX_E_CUDA;
+    GemvItem item;
+    item.chunks = w->chunks_dev;
+    item.x = X_dev;
+    item.y = Y_dev;
+    item.TR = w->rows / 32;
+    item.TC = w->cols / 256;
+    uint8_t* ws = static_cast<uint8_t*>(workspace_dev);
+    return from_cuda(launch_gemv_tokens(w->kind, item, M, out_dtype == Q4NX_OUT_F32, reinterpret_cast<uint32_t*>(ws),
+                                        ws + gemm_part_bytes(w), info, s));
+  }
   return from_cuda(launch_gemm(w->kind, w->chunks_dev, w->rows / 32, w->cols / 256, X_dev, M, Y_dev,
-                               out_dtype == Q4NX_OUT_F32, workspace_dev, static_cast<cudaStream_t>(stream)));
+                               out_dtype == Q4NX_OUT_F32, workspace_dev, s));
 }
 
 int q4nx_pack_q4_1(int src_type, const void* src_dev, uint64_t src_bytes, int64_t rows, int64_t cols, void* out_dev,

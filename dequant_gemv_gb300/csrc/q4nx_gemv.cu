@@ -1,51 +1,50 @@
-// q4nx_gemv.cu -- fused decode + GEMV (one token) over Q4NX chunks, sm_103a.
+// q4nx_gemv.cu -- fused decode + GEMV over Q4NX chunks for one to a few
+// tokens, sm_103a.
 //
-// y[n] = sum_k w[n][k] x[k], weights in the chunk kinds of the "Q4NX chunks"
-// section of the 1bit engine "NPU engine" page (chunk-kind table: q4_1
-// code*scale+zero, Q4_K S*scale*code+M*min, Q8 d*code in layout KR or BLK).
-// One launch runs a batch of independent GEMVs of one chunk kind (a single
-// GEMV is a batch of one).
+// y_m[n] = sum_k w[n][k] x_m[k], weights in the chunk kinds of the "Q4NX
+// chunks" section of the 1bit engine "NPU engine" page (chunk-kind table:
+// q4_1 code*scale+zero, Q4_K S*scale*code+M*min, Q8 d*code in layout KR or
+// BLK).  One launch runs a batch of independent one-token GEMVs of one chunk
+// kind (a single GEMV is a batch of one), or one weight against MT tokens.
 //
-// Design (HBM-bound: 0.625 B/weight for q4_1, so the instruction budget is
-// about three per weight at full bandwidth):
+// Design (HBM-bound: 0.625 B/weight for q4_1):
 //  * Persistent grid, one CTA per SM.  The chunks of all items form one index
-//    space (item after item, each row-major over its tile grid); every warp is
-//    an independent worker owning a contiguous range of it, balanced to within
-//    one chunk.  A range is a run of (item, tile row) segments.
-//  * Each worker streams its chunks with 1-D bulk async copies (TMA
+//    space (item after item, each row-major over its tile grid); CTA b owns an
+//    even contiguous share, each warp a contiguous part of it.  A range is a
+//    run of (item, tile row) segments.
+//  * Each warp streams its chunks with 1-D bulk async copies (TMA
 //    cp.async.bulk) into its own ring of shared-memory stages: the chunk and
-//    the 512-byte bf16 slice of x for the chunk's tile column, completing on
-//    one mbarrier per stage.  Every wait is bounded.  No CTA-wide barrier.
-//  * 4-bit kinds: lane (q = lane>>3, g = lane&7) reads the 16-byte run of 32
-//    codes of group g in row 4i+q (a 512-byte conflict-free LDS.128 per warp
-//    and i).  Codes become floats with one shift-or-LOP3 each: a nibble moved
-//    to bit 15 (even k) or 19 (odd k) of 0x3F800000 is 1 + c*2^-8 or
-//    1 + c*2^-4, so with packed FFMA2 over (even, odd) column pairs
-//        acc_e = X_e + 2^-8 sum_even c x,   acc_o = X_o + 2^-4 sum_odd c x
-//    (X_e, X_o the group's sums of x), and the scale and zero factor out:
-//        y_r += s_rg * ((acc_e - X_e) 2^8 + (acc_o - X_o) 2^4) + z_rg (X_e + X_o).
-//  * Q8 kinds: lane reads 8 rows x 1 column (LDS.64, conflict-free for both
-//    layouts); codes become exact floats through the 2^23 magic number; d_rg
-//    scales each lane's (row, group) partial.
+//    the 512-byte bf16 slices of x for the chunk's tile column, completing on
+//    one mbarrier per stage.  Every wait is bounded.  The chunks are fetched
+//    before the kernel waits on the previous grid (weights never change
+//    between launches); x only after.
+//  * 4-bit kinds: the lanes first read their share of the stage into
+//    registers and the stage is refilled at once; then x becomes 16-bit fixed
+//    point per 32-column group (two byte planes) and the code dot products are
+//    exact dp4a integer sums; scale and zero are applied per (row, group).
+//  * Q8 kinds: codes become exact floats through the 2^23 magic number and
+//    packed fp32 FMAs; d scales each lane's (row, group) partial.
 //  * Row sums are finished with a warp transpose-reduce.  A tile row split
-//    between workers is finished by the last worker to arrive (arrival
-//    counter per tile row in the workspace), which adds the partials in
-//    worker order, clears them, and resets the counter: results do not depend
-//    on timing and the workspace is left zero-filled.
+//    between warps of a CTA is finished by the last of them to arrive (a
+//    shared-memory counter), one split between CTAs by the CTA holding its
+//    first chunk, which reads the others' sums posted as (value, ready flag)
+//    words.  Partials are added in a fixed order, so results do not depend on
+//    timing, and the workspace is left zero-filled.
 #include "q4nx_device.cuh"
 #include "q4nx_kernels.h"
 
 namespace q4nx {
 
-constexpr int kXSliceBytes = 512;            // bf16 x of one tile column
-constexpr int kScratchBytes = 512;           // per warp: x byte planes of one chunk
-constexpr int kSlotBytes = 2 * 32 * 4 + 8;   // per warp: sums of its first and last tile row, 2 counters
+constexpr int kXSliceBytes = 512;            // bf16 x of one tile column, per token
+constexpr int kScratchBytes = 512;           // per warp and token: x byte planes of one chunk
+constexpr int kSlotBytes = 2 * 32 * 4;       // per warp and token: sums of its first and last tile row
+constexpr int kCntBytes = 8;                 // per warp: arrival counters of its first and last tile row
 constexpr int kMaxBatch = kMaxGemvItems;
 
 struct GemvItemDev {
   const uint8_t* chunks;
-  const uint8_t* x;        // bf16 [K]
-  void* y;                 // [N]
+  const uint8_t* x;        // bf16 [K] (token m at x + m * x_stride)
+  void* y;                 // [N] (token m at y + m * y_stride elements)
   int64_t cbase;           // first chunk of this item in the batch index space
   int64_t nchunks;         // TR * TC
   int32_t TC;
@@ -60,9 +59,12 @@ struct GemvArgsT {
   int grid;                // CTAs; CTA b owns chunks [T b / grid, T (b+1) / grid)
   int stages;
   int out_f32;
+  int m;                   // tokens (1 unless one item against several tokens)
+  int64_t x_stride;        // bytes between tokens' x
+  int64_t y_stride;        // elements between tokens' y
   int64_t T;               // chunks in the batch
   uint32_t* err;
-  uint64_t* posted;        // [grid][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
+  uint64_t* posted;        // [grid][MT][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
   // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
   // row) key; the last CTA to finish writes the row index
   int32_t* top1_idx;       // null: store y
@@ -101,6 +103,11 @@ __device__ __forceinline__ int64_t cta_of(int64_t c, int64_t T, int64_t G) { ret
 // Row n's final value (called by all 32 lanes of a warp together, one row
 // each): store it, or in top-1 mode fold it into the CTA's largest key.
 template <class GemvArgs>
+__device__ __forceinline__ void* token_y(const GemvArgs& a, void* y, int tok) {
+  return static_cast<char*>(y) + static_cast<int64_t>(tok) * a.y_stride * (a.out_f32 ? 4 : 2);
+}
+
+template <class GemvArgs>
 __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, float v) {
   if (a.top1_idx) {
     uint64_t key = argmax_key(v, static_cast<uint32_t>(n));
@@ -125,34 +132,45 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
 // words it used.
 constexpr uint64_t kPosted = 1ull << 32;
 
-template <class GemvArgs>
+template <int MT, class GemvArgs>
 __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t Lc, int it, int64_t tr, int64_t r0,
-                                           int64_t r1, float val, int lane) {
+                                           int64_t r1, const float (&val)[MT], int lane) {
   const GemvItemDev& item = a.items[it];
+  const int m = (MT == 1) ? 1 : a.m;
   if (r0 < Lc) {                                      // not the finisher: post
-    st_relaxed_u64(&a.posted[b * 32 + lane], kPosted | __float_as_uint(val));
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) st_relaxed_u64(&a.posted[(b * MT + tok) * 32 + lane], kPosted | __float_as_uint(val[tok]));
     return;
   }
   const int64_t c_last = cta_of(r1 - 1, a.T, a.grid);
-  float sum = val;
+  float sum[MT];
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok) sum[tok] = val[tok];
   for (int64_t c = b + 1; c <= c_last; ++c) {
-    uint64_t* p = &a.posted[c * 32 + lane];
-    uint64_t w = ld_relaxed_u64(p);
-    if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
-      const uint64_t t0 = globaltimer_ns();
-      while ((w & kPosted) == 0) {
-        w = ld_relaxed_u64(p);
-        if ((w & kPosted) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
-      }
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok) {
+      if (tok >= m) break;
+      uint64_t* p = &a.posted[(c * MT + tok) * 32 + lane];
+      uint64_t w = ld_relaxed_u64(p);
       if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
-        if (lane == 0) atomicOr(a.err, 1u);
-        return;
+        const uint64_t t0 = globaltimer_ns();
+        while ((w & kPosted) == 0) {
+          w = ld_relaxed_u64(p);
+          if ((w & kPosted) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+        if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
+          if (lane == 0) atomicOr(a.err, 1u);
+          return;
+        }
       }
+      sum[tok] += __uint_as_float(static_cast<uint32_t>(w));
+      *p = 0ull;                                      // leave the workspace zero-filled
     }
-    sum += __uint_as_float(static_cast<uint32_t>(w));
-    *p = 0ull;                                        // leave the workspace zero-filled
   }
-  store_y(a, item.y, tr * 32 + lane, sum);
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok)
+    if (tok < m) store_y(a, token_y(a, item.y, tok), tr * 32 + lane, sum[tok]);
 }
 
 // ------------------------------------------------------- chunk bodies ----
@@ -182,21 +200,23 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // A q4 chunk's share of one lane, read out of the ring stage at once so that
 // the stage can be refilled before the arithmetic starts.  Prep lane
 // (gp = lane & 7, tp = lane >> 3) reads the 8 columns gp*32 + 8tp .. +7 of
-// the x slice (code word tp of group gp); decode lane (qr = lane >> 3,
-// g = lane & 7) reads rows 4i + qr of group g: 16 code bytes and the
-// group's scale fields per row.
-template <int KIND>
+// each token's x slice (code word tp of group gp); decode lane (qr = lane >> 3,
+// g = lane & 7) reads rows 4i + qr of group g: 16 code bytes and the group's
+// scale fields per row.
+template <int KIND, int MT>
 struct Q4Lane {
-  uint4 xr;
+  uint4 xr[MT];
   uint4 cw[8];
   uint32_t f0[8], f1[8];           // q4_1: scale, zero bits; Q4_K: S bits | M bits << 16, sc | mn << 16
 };
 
-template <int KIND>
-__device__ __forceinline__ void q4_read(uint32_t st, int lane, Q4Lane<KIND>& L) {
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_read(uint32_t st, int lane, int m, Q4Lane<KIND, MT>& L) {
   constexpr int CB = chunk_bytes_of(KIND);
   const int gp = lane & 7, tp = lane >> 3;
-  L.xr = lds128(st + CB + gp * 64 + tp * 16);
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok)
+    if (tok < m) L.xr[tok] = lds128(st + CB + tok * kXSliceBytes + gp * 64 + tp * 16);
   const int qr = lane >> 3, g = lane & 7;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -212,11 +232,12 @@ __device__ __forceinline__ void q4_read(uint32_t st, int lane, Q4Lane<KIND>& L) 
   }
 }
 
-template <int KIND>
-__device__ __forceinline__ void q4_compute(const Q4Lane<KIND>& L, uint32_t scratch, int lane, float (&yacc)[8]) {
-  // ---- x slice -> byte planes
+// One token's x slice (this prep lane's 8 columns) -> byte planes in the
+// warp's scratch; returns the group's sum X_g (g = lane & 7) and sets
+// inv = 2^(E_g - 141).
+__device__ __forceinline__ float q4_x_planes(const uint4 xr, uint32_t scratch, int lane, float& inv) {
   const int gp = lane & 7, tp = lane >> 3;
-  const uint32_t xw[4] = {L.xr.x, L.xr.y, L.xr.z, L.xr.w};
+  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
   uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
                          __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
   uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
@@ -224,7 +245,7 @@ __device__ __forceinline__ void q4_compute(const Q4Lane<KIND>& L, uint32_t scrat
   mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
   const int E = max(static_cast<int>(mx >> 7), 15);             // biased exponent of the group's max |x|
   const float scale = __int_as_float((268 - E) << 23);          // 2^(141 - E)
-  const float inv = __int_as_float((E - 14) << 23);             // 2^(E - 141)
+  inv = __int_as_float((E - 14) << 23);                         // 2^(E - 141)
   float xs = 0.f;
   int q[8];
 #pragma unroll
@@ -244,12 +265,25 @@ __device__ __forceinline__ void q4_compute(const Q4Lane<KIND>& L, uint32_t scrat
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(p0e), "r"(p0o),
                "r"(p1e), "r"(p1o)
                : "memory");
-  __syncwarp();
-  // ---- decode lane: rows 4i + qr of group g
-  const int g = lane & 7;
-  uint4 P[4];
+  return xs;
+}
+
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_compute(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
+                                           float (&yacc)[MT][8]) {
+  float xs[MT], inv[MT];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) P[t] = lds128(scratch + (t * 8 + g) * 16);
+  for (int tok = 0; tok < MT; ++tok)
+    if (tok < m) xs[tok] = q4_x_planes(L.xr[tok], scratch + tok * kScratchBytes, lane, inv[tok]);
+  __syncwarp();
+  // ---- decode lane: rows 4i + qr of group g; every token's planes at hand
+  const int g = lane & 7;
+  uint4 P[MT][4];
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok)
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (tok < m) P[tok][t] = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
   __syncwarp();                                                 // scratch is rewritten by the next chunk
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -262,18 +296,27 @@ __device__ __forceinline__ void q4_compute(const Q4Lane<KIND>& L, uint32_t scrat
       z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
     }
     const uint32_t w[4] = {L.cw[i].x, L.cw[i].y, L.cw[i].z, L.cw[i].w};
-    uint32_t s0 = 0;
-    int s1 = 0;
+    uint32_t lo[4], hi[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t lo = w[t] & 0x0F0F0F0Fu, hi = (w[t] >> 4) & 0x0F0F0F0Fu;
-      s0 = dp4a_uu(lo, P[t].x, s0);
-      s0 = dp4a_uu(hi, P[t].y, s0);
-      s1 = dp4a_us(lo, P[t].z, s1);
-      s1 = dp4a_us(hi, P[t].w, s1);
+      lo[t] = w[t] & 0x0F0F0F0Fu;
+      hi[t] = (w[t] >> 4) & 0x0F0F0F0Fu;
     }
-    const float dot = __int2float_rn(s1 * 256 + static_cast<int>(s0));   // exact: |.| < 2^24
-    yacc[i] = fmaf(s * inv, dot, fmaf(z, xs, yacc[i]));
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok) {
+      if (tok >= m) break;
+      uint32_t s0 = 0;
+      int s1 = 0;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        s0 = dp4a_uu(lo[t], P[tok][t].x, s0);
+        s0 = dp4a_uu(hi[t], P[tok][t].y, s0);
+        s1 = dp4a_us(lo[t], P[tok][t].z, s1);
+        s1 = dp4a_us(hi[t], P[tok][t].w, s1);
+      }
+      const float dot = __int2float_rn(s1 * 256 + static_cast<int>(s0));   // exact: |.| < 2^24
+      yacc[tok][i] = fmaf(s * inv[tok], dot, fmaf(z, xs[tok], yacc[tok][i]));
+    }
   }
 }
 
@@ -284,8 +327,8 @@ __device__ __forceinline__ void q8_lane_map(int lane, int& qe, int& kc) {
   else { qe = ((lane >> 4) << 1) | (lane & 1); kc = (lane >> 1) & 7; }
 }
 
-template <int KIND>
-__device__ __forceinline__ void q8_chunk(uint32_t st, int lane, float (&yacc)[8]) {
+template <int KIND, int MT>
+__device__ __forceinline__ void q8_chunk(uint32_t st, int lane, int m, float (&yacc)[MT][8]) {
   int qe, kc;
   q8_lane_map<KIND>(lane, qe, kc);
   const float MAGIC = 8388736.0f;   // 2^23 + 128: float(2^23 + (c ^ 0x80)) - MAGIC == c exactly
@@ -296,7 +339,11 @@ __device__ __forceinline__ void q8_chunk(uint32_t st, int lane, float (&yacc)[8]
   for (int i = 0; i < 8; ++i) drow[i] = lds128(st + kQ8D + (qe * 8 + i) * 16);
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 acc[MT][4];
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[tok][u] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int tt = 0; tt < 4; ++tt) {
       const int kk = 8 * tt + kc;                 // column within the group
@@ -304,24 +351,31 @@ __device__ __forceinline__ void q8_chunk(uint32_t st, int lane, float (&yacc)[8]
       if constexpr (KIND == kQ8_KR) off = (g * 32 + kk) * 32 + qe * 8;
       else off = (qe >> 1) * 4096 + g * 512 + kk * 16 + (qe & 1) * 8;
       const uint2 cw = lds64(st + off);
-      const float xk = bf16_bits_to_f32(lds_u16(st + kQ8Bytes + (g * 32 + kk) * 2));
-      const float2 xx = make_float2(xk, xk);
       const uint32_t w0 = cw.x ^ 0x80808080u, w1 = cw.y ^ 0x80808080u;
       float2 c01 = fadd2(make_float2(__uint_as_float(prmt(w0, B, 0x7540)), __uint_as_float(prmt(w0, B, 0x7541))), nm);
       float2 c23 = fadd2(make_float2(__uint_as_float(prmt(w0, B, 0x7542)), __uint_as_float(prmt(w0, B, 0x7543))), nm);
       float2 c45 = fadd2(make_float2(__uint_as_float(prmt(w1, B, 0x7540)), __uint_as_float(prmt(w1, B, 0x7541))), nm);
       float2 c67 = fadd2(make_float2(__uint_as_float(prmt(w1, B, 0x7542)), __uint_as_float(prmt(w1, B, 0x7543))), nm);
-      acc[0] = ffma2(c01, xx, acc[0]);
-      acc[1] = ffma2(c23, xx, acc[1]);
-      acc[2] = ffma2(c45, xx, acc[2]);
-      acc[3] = ffma2(c67, xx, acc[3]);
+#pragma unroll
+      for (int tok = 0; tok < MT; ++tok) {
+        if (tok >= m) break;
+        const float xk = bf16_bits_to_f32(lds_u16(st + kQ8Bytes + tok * kXSliceBytes + (g * 32 + kk) * 2));
+        const float2 xx = make_float2(xk, xk);
+        acc[tok][0] = ffma2(c01, xx, acc[tok][0]);
+        acc[tok][1] = ffma2(c23, xx, acc[tok][1]);
+        acc[tok][2] = ffma2(c45, xx, acc[tok][2]);
+        acc[tok][3] = ffma2(c67, xx, acc[tok][3]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t wd = (g >> 1) == 0 ? drow[i].x : (g >> 1) == 1 ? drow[i].y : (g >> 1) == 2 ? drow[i].z : drow[i].w;
       const float d = __uint_as_float((g & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-      const float part = (i & 1) ? acc[i >> 1].y : acc[i >> 1].x;
-      yacc[i] = fmaf(d, part, yacc[i]);
+#pragma unroll
+      for (int tok = 0; tok < MT; ++tok) {
+        const float part = (i & 1) ? acc[tok][i >> 1].y : acc[tok][i >> 1].x;
+        yacc[tok][i] = fmaf(d, part, yacc[tok][i]);
+      }
     }
   }
 }
@@ -376,24 +430,28 @@ __device__ __forceinline__ int warp_of(int64_t c, int64_t Lc, int64_t Hc, int nw
 }
 
 // End of a segment (item it, tile row tr) of warp w (range [lo, hi)); each
-// lane holds the sum of the row `row`.  A row held by this warp alone is
-// stored at once.  A row shared with other warps of the CTA is parked in the
-// warp's slot (0: its first segment, 1: its last); the last of those warps to
-// arrive (shared-memory counter of the row's first warp) adds the slots in
-// warp order and stores y, or hands the row on to cross_cta_row when other
-// CTAs share it too.
-template <class GemvArgs>
+// lane holds, per token, the sum of the row `row`.  A row held by this warp
+// alone is stored at once.  A row shared with other warps of the CTA is parked
+// in the warp's slot (0: its first segment, 1: its last); the last of those
+// warps to arrive (shared-memory counter of the row's first warp) adds the
+// slots in warp order and stores y, or hands the row on to cross_cta_row when
+// other CTAs share it too.
+template <int MT, class GemvArgs>
 __device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_t Lc, int64_t Hc, int w, int nw,
-                                            int64_t lo, int64_t hi, int it, int64_t tr, int row, float val, float* slots,
-                                            uint32_t* cnt, int lane) {
+                                            int64_t lo, int64_t hi, int it, int64_t tr, int row,
+                                            const float (&val)[MT], float* slots, uint32_t* cnt, int lane) {
   const GemvItemDev& item = a.items[it];
+  const int m = (MT == 1) ? 1 : a.m;
   const int64_t r0 = item.cbase + tr * item.TC, r1 = r0 + item.TC;
   if (lo <= r0 && r1 <= hi) {
-    store_y(a, item.y, tr * 32 + row, val);
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) store_y(a, token_y(a, item.y, tok), tr * 32 + row, val[tok]);
     return;
   }
   const int k = (r0 <= lo) ? 0 : 1;                 // the warp's first segment iff the row holds lo
-  slots[(w * 2 + k) * 32 + row] = val;
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok) slots[((w * 2 + k) * MT + tok) * 32 + row] = val[tok];
   const int wa = warp_of(r0 > Lc ? r0 : Lc, Lc, Hc, nw);
   const int wb = warp_of((r1 < Hc ? r1 : Hc) - 1, Lc, Hc, nw);
   const int64_t lo_a = Lc + ((Hc - Lc) * wa) / nw;
@@ -405,31 +463,54 @@ __device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != static_cast<uint32_t>(wb - wa)) return;   // another warp of the CTA finishes the row
   __threadfence_block();
-  float sum = slots[(wa * 2 + ka) * 32 + lane];
-  for (int v = wa + 1; v <= wb; ++v) sum += slots[(v * 2) * 32 + lane];
-  if (r0 >= Lc && r1 <= Hc) store_y(a, item.y, tr * 32 + lane, sum);
-  else cross_cta_row(a, b, Lc, it, tr, r0, r1, sum, lane);
+  float sum[MT];
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok) {
+    sum[tok] = slots[((wa * 2 + ka) * MT + tok) * 32 + lane];
+    for (int v = wa + 1; v <= wb; ++v) sum[tok] += slots[((v * 2) * MT + tok) * 32 + lane];
+  }
+  if (r0 >= Lc && r1 <= Hc) {
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) store_y(a, token_y(a, item.y, tok), tr * 32 + lane, sum[tok]);
+  } else {
+    cross_cta_row<MT>(a, b, Lc, it, tr, r0, r1, sum, lane);
+  }
 }
 
-template <int KIND, class GemvArgs>
-__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
+template <int KIND, int MT, class GemvArgs>
+__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  mbar_arrive_expect_tx(bar, CB + kXSliceBytes);
+  mbar_arrive_expect_tx(bar, CB + m * kXSliceBytes);
   bulk_g2s(dst, a.items[p.it].chunks + p.local * CB, CB, bar);
 }
-template <int KIND, class GemvArgs>
-__device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, uint8_t* dst, uint64_t* bar) {
+template <int KIND, int MT, class GemvArgs>
+__device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  bulk_g2s(dst + CB, a.items[p.it].x + static_cast<int64_t>(p.tc) * kXSliceBytes, kXSliceBytes, bar);
+  const uint8_t* x = a.items[p.it].x + static_cast<int64_t>(p.tc) * kXSliceBytes;
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok)
+    if (tok < m) bulk_g2s(dst + CB + tok * kXSliceBytes, x + tok * a.x_stride, kXSliceBytes, bar);
 }
 
-template <int KIND, int MAXB>
-__global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
+// Threads per CTA the kernel is compiled for.  One token: at most 128
+// registers, so that two CTAs of 8 warps share an SM (consecutive launches
+// overlap).  Two tokens of a 4-bit kind: 12 warps, the most that the tokens'
+// registers allow, to hide the latency of the integer dot products.
+// Otherwise 8 warps with the register budget of a lone CTA.
+template <int KIND, int MT>
+constexpr int gemv_max_threads() {
+  return MT == 1 ? 512 : (MT == 2 && (KIND == kQ4_1 || KIND == kQ4_K)) ? 384 : 256;
+}
+
+template <int KIND, int MAXB, int MT>
+__global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int SB = chunk_bytes_of(KIND) + kXSliceBytes;     // stage bytes
+  constexpr int SB = chunk_bytes_of(KIND) + MT * kXSliceBytes;     // stage bytes
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int m = (MT == 1) ? 1 : a.m;
   const int64_t b = blockIdx.x;
   const int64_t Lc = (a.T * b) / a.grid, Hc = (a.T * (b + 1)) / a.grid;
   const int64_t lo = Lc + ((Hc - Lc) * warp) / nwarps, hi = Lc + ((Hc - Lc) * (warp + 1)) / nwarps;
@@ -438,9 +519,9 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   uint8_t* ring = smem + static_cast<uint64_t>(warp) * stages * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * stages;
   uint8_t* tail = smem + ring_bytes + align16(static_cast<uint64_t>(nwarps) * stages * 8);
-  const uint32_t scratch = smem_u32(tail) + warp * kScratchBytes;
-  float* slots = reinterpret_cast<float*>(tail + nwarps * kScratchBytes);   // [nwarps][2][32]
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(slots + nwarps * 64);         // [nwarps][2]
+  const uint32_t scratch = smem_u32(tail) + warp * MT * kScratchBytes;
+  float* slots = reinterpret_cast<float*>(tail + nwarps * MT * kScratchBytes);   // [nwarps][2][MT][32]
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(slots + nwarps * 2 * MT * 32);     // [nwarps][2]
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur{}, pre{};                         // chunk being processed / next chunk to fetch
@@ -452,14 +533,14 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     // weights never change between launches: fetch the first chunks before waiting on the previous grid
     Pos p = pre;
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_chunk<KIND>(a, p, ring + s * SB, &bars[s]);
+      issue_chunk<KIND, MT>(a, p, m, ring + s * SB, &bars[s]);
       p.next(a);
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
   if (lane == 0) {
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_xslice<KIND>(a, pre, ring + s * SB, &bars[s]);
+      issue_xslice<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
       pre.next(a);
     }
   }
@@ -468,9 +549,11 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
   __syncwarp();
   __syncthreads();                          // the row counters are zero before any warp can count
 
-  float yacc[8];
+  float yacc[MT][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
+  for (int tok = 0; tok < MT; ++tok)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) yacc[tok][i] = 0.f;
   int seg_it = cur.it, seg_tr = cur.tr;
   uint32_t phase = 0;                       // bit s: parity awaited next on stage s
   int s = 0;
@@ -482,26 +565,30 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     phase ^= 1u << s;
     if (cur.it != seg_it || cur.tr != seg_tr) {    // the previous segment is complete
       int row;
-      const float v = finish_rows<KIND>(yacc, lane, row);
-      finish_segment(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
+      float v[MT];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) yacc[i] = 0.f;
+      for (int tok = 0; tok < MT; ++tok) v[tok] = finish_rows<KIND>(yacc[tok], lane, row);
+      finish_segment<MT>(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
+#pragma unroll
+      for (int tok = 0; tok < MT; ++tok)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yacc[tok][i] = 0.f;
       seg_it = cur.it;
       seg_tr = cur.tr;
     }
     const uint32_t st = smem_u32(ring + s * SB);
     // 4-bit chunks: the lanes take their share of the stage into registers
     // and the stage is refilled before the arithmetic; Q8: after it
-    Q4Lane<Q4 ? KIND : kQ4_1> q4l;
-    if constexpr (Q4) q4_read<KIND>(st, lane, q4l);
-    else q8_chunk<KIND>(st, lane, yacc);
+    Q4Lane<Q4 ? KIND : kQ4_1, MT> q4l;
+    if constexpr (Q4) q4_read<KIND, MT>(st, lane, m, q4l);
+    else q8_chunk<KIND, MT>(st, lane, m, yacc);
     __syncwarp();
     if (lane == 0 && j + stages < n) {
-      issue_chunk<KIND>(a, pre, ring + s * SB, &bars[s]);
-      issue_xslice<KIND>(a, pre, ring + s * SB, &bars[s]);
+      issue_chunk<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
+      issue_xslice<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
       pre.next(a);
     }
-    if constexpr (Q4) q4_compute<KIND>(q4l, scratch, lane, yacc);
+    if constexpr (Q4) q4_compute<KIND, MT>(q4l, scratch, lane, m, yacc);
     cur.next(a);
     if (++s == stages) s = 0;
   }
@@ -511,10 +598,12 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
     for (int t = 0; t < stages; ++t) mbar_wait_bounded(&bars[t], (phase >> t) & 1u, 100000000ull);
   } else {
     int row;
-    const float v = finish_rows<KIND>(yacc, lane, row);
-    finish_segment(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
+    float v[MT];
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok) v[tok] = finish_rows<KIND>(yacc[tok], lane, row);
+    finish_segment<MT>(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
   }
-  if (a.top1_idx) {
+  if (MT == 1 && a.top1_idx) {
     // every warp's rows are folded in; the CTA's key goes to the launch's key,
     // and the last CTA to finish writes the index and clears the two words
     __syncthreads();
@@ -534,13 +623,18 @@ __global__ void __launch_bounds__(512, 1) gemv_kernel(const __grid_constant__ Ge
 
 // ----------------------------------------------------------------- host ----
 
-bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
+static int gemv_max_warps(int kind, int MT) {
+  const bool q4 = kind == kQ4_1 || kind == kQ4_K;
+  return MT == 1 ? 8 : (MT == 2 && q4) ? 12 : 8;
+}
+
+bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT) {
   const int CB = chunk_bytes_of(kind);
-  if (CB == 0 || info.sms <= 0 || T <= 0) return false;
-  const uint64_t SB = static_cast<uint64_t>(CB) + kXSliceBytes;
+  if (CB == 0 || info.sms <= 0 || T <= 0 || MT < 1) return false;
+  const uint64_t SB = static_cast<uint64_t>(CB) + static_cast<uint64_t>(MT) * kXSliceBytes;
   auto need = [&](int w, int st) {
     return static_cast<uint64_t>(w) * st * SB + align16(static_cast<uint64_t>(w) * st * 8) +
-           static_cast<uint64_t>(w) * (kScratchBytes + kSlotBytes);
+           static_cast<uint64_t>(w) * (MT * (kScratchBytes + kSlotBytes) + kCntBytes);
   };
   // Eight warps per CTA, each streaming a longer run of chunks, measured best
   // on GB300 against 12 and 16.  4-bit chunks: the CTA stays within half an
@@ -549,10 +643,15 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
   // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
   // chunks are larger and gain more from a deeper ring than from that overlap.
   // (less 64 bytes for the kernel's static shared memory)
-  const uint64_t cap = static_cast<uint64_t>(CB <= kQ41Bytes ? info.smem_two_per_sm : info.max_smem_optin) - 64;
-  static const int kWarpChoices[] = {8, 6, 4, 2, 1};
+  // Several tokens need more registers than two CTAs per SM leave, so those
+  // launches take the whole of the shared memory.
+  const uint64_t cap =
+      static_cast<uint64_t>(CB <= kQ41Bytes && MT == 1 ? info.smem_two_per_sm : info.max_smem_optin) - 64;
+  const int max_warps = gemv_max_warps(kind, MT);
+  static const int kWarpChoices[] = {12, 8, 6, 4, 2, 1};
   int warps = 0, stages = 0;
   for (int w : kWarpChoices) {
+    if (w > max_warps) continue;
     for (int st = 4; st >= 2; --st) {
       if (need(w, st) <= cap) { warps = w; stages = st; break; }
     }
@@ -574,16 +673,16 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p) {
   return true;
 }
 
-uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks) {
+uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int MT) {
   (void)total_chunks;
   (void)total_tile_rows;
-  return kWsErrBytes + static_cast<uint64_t>(kMaxCtas) * 32 * 8;
+  return kWsErrBytes + static_cast<uint64_t>(kMaxCtas) * MT * 32 * 8;
 }
 
-template <int KIND, int MAXB>
+template <int KIND, int MAXB, int MT>
 static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
-  const int slot = KIND + (MAXB == 1 ? 0 : MAXB == 8 ? 4 : 8);
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB>), slot);
+  const int slot = MT == 1 ? KIND + (MAXB == 1 ? 0 : MAXB == 8 ? 4 : 8) : (MT == 2 ? 20 : 24) + KIND;
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT>), slot);
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: SMs freed by the previous grid start this
   // one at once; the kernel waits for the previous grid before touching x, y
@@ -598,15 +697,13 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB>, a);
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB, MT>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int MAXB>
-static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
-                                     const DeviceInfo& info, int32_t* top1_idx, cudaStream_t s) {
-  GemvArgsT<MAXB> a;
+static void fill_items(GemvArgsT<MAXB>& a, const GemvItem* items, int n) {
   int64_t T = 0;
   for (int i = 0; i < n; ++i) {
     a.items[i].chunks = static_cast<const uint8_t*>(items[i].chunks);
@@ -617,24 +714,39 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
     a.items[i].TC = static_cast<int32_t>(items[i].TC);
     T += items[i].TR * items[i].TC;
   }
-  GemvPlan p;
-  if (!gemv_plan(kind, T, info, &p)) return cudaErrorInvalidValue;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.nitems = n;
-  a.grid = p.grid;
-  a.stages = p.stages;
-  a.out_f32 = out_f32;
   a.T = T;
+}
+
+template <int MAXB>
+static void fill_workspace(GemvArgsT<MAXB>& a, void* workspace) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.err = reinterpret_cast<uint32_t*>(ws);
-  a.top1_idx = top1_idx;
   a.top1_done = reinterpret_cast<uint32_t*>(ws + 4);
   a.top1_key = reinterpret_cast<uint64_t*>(ws + 8);
   a.posted = reinterpret_cast<uint64_t*>(ws + kWsErrBytes);
+}
+
+template <int MAXB>
+static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
+                                     const DeviceInfo& info, int32_t* top1_idx, cudaStream_t s) {
+  GemvArgsT<MAXB> a;
+  fill_items(a, items, n);
+  GemvPlan p;
+  if (!gemv_plan(kind, a.T, info, &p, 1)) return cudaErrorInvalidValue;
+  fill_workspace(a, workspace);
+  a.grid = p.grid;
+  a.stages = p.stages;
+  a.out_f32 = out_f32;
+  a.m = 1;
+  a.x_stride = 0;
+  a.y_stride = 0;
+  a.top1_idx = top1_idx;
   switch (kind) {
-    case kQ4_1: return launch_gemv_t<kQ4_1, MAXB>(a, p, s);
-    case kQ4_K: return launch_gemv_t<kQ4_K, MAXB>(a, p, s);
-    case kQ8_KR: return launch_gemv_t<kQ8_KR, MAXB>(a, p, s);
-    case kQ8_BLK: return launch_gemv_t<kQ8_BLK, MAXB>(a, p, s);
+    case kQ4_1: return launch_gemv_t<kQ4_1, MAXB, 1>(a, p, s);
+    case kQ4_K: return launch_gemv_t<kQ4_K, MAXB, 1>(a, p, s);
+    case kQ8_KR: return launch_gemv_t<kQ8_KR, MAXB, 1>(a, p, s);
+    case kQ8_BLK: return launch_gemv_t<kQ8_BLK, MAXB, 1>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -650,6 +762,58 @@ cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f3
 cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
                              cudaStream_t s) {
   return launch_gemv_sized<1>(kind, &item, 1, 1, workspace, info, idx, s);
+}
+
+int gemv_max_tokens(int kind) {
+  switch (kind) {
+    case kQ4_1: return kGemvTokensQ41;
+    case kQ4_K: return kGemvTokensQ4K;
+    case kQ8_KR:
+    case kQ8_BLK: return kGemvTokensQ8;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f32, uint32_t* err, void* workspace,
+                               const DeviceInfo& info, cudaStream_t s) {
+  if (M < 1 || M > gemv_max_tokens(kind)) return cudaErrorInvalidValue;
+  const int MT = M == 1 ? 1 : M == 2 ? 2 : 4;
+  GemvArgsT<1> a;
+  fill_items(a, &item, 1);
+  GemvPlan p;
+  if (!gemv_plan(kind, a.T, info, &p, MT)) return cudaErrorInvalidValue;
+  fill_workspace(a, workspace);
+  a.err = err;
+  a.grid = p.grid;
+  a.stages = p.stages;
+  a.out_f32 = out_f32;
+  a.m = M;
+  a.x_stride = item.TC * 256 * 2;                 // X rows: cols bf16 each
+  a.y_stride = item.TR * 32;                      // Y rows: rows elements each
+  a.top1_idx = nullptr;
+  if (MT == 1) {                                  // one token: the single-GEMV kernel itself
+    switch (kind) {
+      case kQ4_1: return launch_gemv_t<kQ4_1, 1, 1>(a, p, s);
+      case kQ4_K: return launch_gemv_t<kQ4_K, 1, 1>(a, p, s);
+      case kQ8_KR: return launch_gemv_t<kQ8_KR, 1, 1>(a, p, s);
+      case kQ8_BLK: return launch_gemv_t<kQ8_BLK, 1, 1>(a, p, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (MT == 2) {
+    switch (kind) {
+      case kQ4_1: return launch_gemv_t<kQ4_1, 1, 2>(a, p, s);
+      case kQ4_K: return launch_gemv_t<kQ4_K, 1, 2>(a, p, s);
+      case kQ8_KR: return launch_gemv_t<kQ8_KR, 1, 2>(a, p, s);
+      case kQ8_BLK: return launch_gemv_t<kQ8_BLK, 1, 2>(a, p, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (kind) {
+    case kQ4_1: return launch_gemv_t<kQ4_1, 1, 4>(a, p, s);
+    case kQ4_K: return launch_gemv_t<kQ4_K, 1, 4>(a, p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace q4nx

@@ -33,8 +33,8 @@ struct GemvPlan {
   int grid = 0;        // CTAs, each owning a contiguous range of chunks
   size_t smem = 0;     // dynamic shared memory bytes
 };
-bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan);
-uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks);
+bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan, int tokens);
+uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int tokens = 1);
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                               const DeviceInfo& info, cudaStream_t s);
 
@@ -43,6 +43,17 @@ cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f3
 // The workspace's bytes 4..15 hold the launch's top-1 words (zero between launches).
 cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
                              cudaStream_t s);
+
+// ---- GEMV of one weight against M tokens (X [M][cols], Y [M][rows]) ----
+// Each chunk is read once for all M tokens.  M up to gemv_max_tokens(kind),
+// the M up to which this beats the tensor-core GEMM on GB300 (measured: two
+// tokens for q4_1 and Q8); Q4_K has no tensor-core path, so it goes to four.
+// `workspace`: gemv_workspace_bytes(.., .., 4) bytes, zero-filled and left
+// so; `err`: the error word to report a failed wait in.
+constexpr int kGemvTokensQ41 = 2, kGemvTokensQ4K = 4, kGemvTokensQ8 = 2, kGemvTokensMax = 4;
+int gemv_max_tokens(int kind);
+cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f32, uint32_t* err, void* workspace,
+                               const DeviceInfo& info, cudaStream_t s);
 
 // ---- standalone decode ----
 cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s);

@@ -141,15 +141,20 @@ uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
 /* Fused decode + GEMM for a block of 1..64 tokens on the tcgen05 tensor cores:
  *   Y[m][n] = sum_k X[m][k] * w[n][k],  m < M.
  * X_dev: bf16 [M][cols] row-major.  Y_dev: [M][rows] row-major of out_dtype.
- * Weights are decoded to bf16 (code*scale + zero for q4_1, rounded once; d*code
- * for Q8, exactly the standalone decode) into tensor memory and multiplied with
- * fp32 accumulation there.  Kinds: q4_1, Q8_KR, Q8_BLK.  Q4_K returns
- * Q4NX_E_UNSUPPORTED (repack it with q4nx_repack_q4k first, which keeps the
- * codes).  The launch expects its CTAs (at most one per SM) to be resident
- * together, as they are when no other kernel occupies the GPU; a stalled
- * launch gives up after a bounded wait and reports it through q4nx_check.
- * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes, zero-filled before
- * first use (it holds the error word). */
+ * A few tokens (M <= 2, or M <= 4 for Q4_K) run on the CUDA cores: each chunk
+ * is read once and its codes enter exact integer (4-bit) or fp32 (Q8) dot
+ * products with every token, as in q4nx_gemv (M = 1 is q4nx_gemv's kernel).  Larger M runs on
+ * the tensor cores: weights are decoded to bf16 (code*scale + zero for q4_1,
+ * rounded once; d*code for Q8, exactly the standalone decode) into tensor
+ * memory and multiplied with fp32 accumulation there; kinds q4_1, Q8_KR,
+ * Q8_BLK, while Q4_K returns Q4NX_E_UNSUPPORTED (repack it with
+ * q4nx_repack_q4k first, which keeps the codes).  The tensor-core launch
+ * expects its CTAs (at most one per SM) to be resident together, as they are
+ * when no other kernel occupies the GPU; a stalled launch gives up after a
+ * bounded wait and reports it through q4nx_check.
+ * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes (the same for every
+ * M), zero-filled before first use; it holds the error word, and calls may
+ * leave partial sums in it, so it is not shared with the GEMV entry points. */
 int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, int out_dtype,
                   void* workspace_dev, uint64_t workspace_bytes, void* stream);
 uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M);

@@ -41,7 +41,7 @@ def run(q, kind, N, K, M, out="f32", rows=None, seed=0, wid=4):
 
 
 @pytest.mark.parametrize("N,K", [(128, 512), (96, 768), (256, 1024), (1024, 1024), (160, 2816), (4224, 512)])
-@pytest.mark.parametrize("M", [64, 1, 17])
+@pytest.mark.parametrize("M", [64, 1, 5, 17])
 def test_gemm_q4_1_small(q, N, K, M):
     run(q, synth.Q4_1, N, K, M)
 
@@ -101,7 +101,7 @@ def test_gemm_matches_gemv_per_token(q):
 
 @pytest.mark.parametrize("kind", [synth.Q8_KR, synth.Q8_BLK])
 @pytest.mark.parametrize("N,K", [(128, 512), (256, 1024), (4224, 512), (160, 2816)])
-@pytest.mark.parametrize("M", [64, 1, 17])
+@pytest.mark.parametrize("M", [64, 1, 5, 17])
 def test_gemm_q8_small(q, kind, N, K, M):
     run(q, kind, N, K, M, wid=5)
 
