@@ -69,6 +69,7 @@ def _load():
         "q4nx_gemv": ([W, P, P, I, P, U64, P], I),
         "q4nx_gemv_workspace": ([W], U64),
         "q4nx_gemv_top1": ([W, P, P, P, U64, P], I),
+        "q4nx_gemv_top1_key": ([W, P, I64, P, P, U64, P], I),
         "q4nx_gemv_batch": ([ctypes.POINTER(q4nx_gemv_item), I, I, P, U64, P], I),
         "q4nx_gemv_batch_workspace": ([ctypes.POINTER(q4nx_gemv_item), I], U64),
         "q4nx_gemm_m64": ([W, P, I, P, I, P, U64, P], I),
@@ -89,7 +90,7 @@ def _load():
 
 lib = _load()
 EXPORTS = ("q4nx_chunk_bytes", "q4nx_status_str", "q4nx_abi_version", "q4nx_decode", "q4nx_gemv",
-           "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_pack_q4_1", "q4nx_argmax",
+           "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_top1_key", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_pack_q4_1", "q4nx_argmax",
            "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes")
 
 
@@ -123,6 +124,13 @@ class Weight:
         tc = self.cols // 256
         cb = q4nx_chunk_bytes(self.kind)
         return Weight(self.chunks[tr0 * tc * cb:(tr0 + count) * tc * cb], self.kind, count * 32, self.cols)
+
+    def row_shard(self, rank: int, world: int) -> tuple["Weight", int]:
+        """Rank `rank`'s share of the rows when `world` devices split the weight by
+        tile rows (contiguous, sizes within one tile row of each other): the
+        shard as a weight of its own and its first global row."""
+        tr0, tr1 = shard_tile_rows(self.rows // 32, rank, world)
+        return self.tile_rows(tr0, tr1 - tr0), tr0 * 32
 
 
 def _stream(dev: torch.device) -> int:
@@ -222,6 +230,57 @@ def q4nx_gemv_top1(w: Weight, x: torch.Tensor, out: torch.Tensor | None = None,
         _check(lib.q4nx_gemv_top1(ctypes.byref(cw), x.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
                                   _stream(w.device)), "q4nx_gemv_top1")
     return out
+
+
+def q4nx_gemv_top1_key(w: Weight, x: torch.Tensor, row_base: int = 0, out: torch.Tensor | None = None,
+                       ws: torch.Tensor | None = None) -> torch.Tensor:
+    """int64 [1]: this shard's top-1 key (q4nx.h), rows numbered from row_base;
+    the keys of all shards combine by a MAX reduction (top1_key_row decodes)."""
+    _cuda(w.chunks, "chunks")
+    _cuda(x, "x")
+    if x.dtype != torch.bfloat16 or x.numel() != w.cols:
+        raise ValueError("x must be bf16 with cols elements")
+    with torch.cuda.device(w.device):
+        if out is None:
+            out = torch.empty(1, dtype=torch.int64, device=w.device)
+        _cuda(out, "out")
+        cw = w.c()
+        need = int(lib.q4nx_gemv_workspace(ctypes.byref(cw)))
+        if ws is None:
+            ws = workspace(w.device, need)
+        _check(lib.q4nx_gemv_top1_key(ctypes.byref(cw), x.data_ptr(), int(row_base), out.data_ptr(), ws.data_ptr(),
+                                      ws.numel(), _stream(w.device)), "q4nx_gemv_top1_key")
+    return out
+
+
+# ---- host side of the sharded lm_head (no GPU work) ----
+
+def shard_tile_rows(tile_rows: int, rank: int, world: int) -> tuple[int, int]:
+    """[first, end) tile rows of `rank` when `world` devices split `tile_rows` tile rows."""
+    if not 0 <= rank < world:
+        raise ValueError("rank outside 0..world-1")
+    return tile_rows * rank // world, tile_rows * (rank + 1) // world
+
+
+def top1_key(value: float, row: int) -> int:
+    """The key format of q4nx_gemv_top1_key for an fp32 `value` at global `row`
+    (for combining keys on the host and for tests of the exchange)."""
+    import struct
+
+    v = float(value)
+    if v != v:
+        ord_ = 0xFFFFFFFF
+    else:
+        b = struct.unpack("<I", struct.pack("<f", 0.0 if v == 0.0 else v))[0]   # rounds to fp32
+        ord_ = (~b & 0xFFFFFFFF) if b & 0x80000000 else (b | 0x80000000)
+    key = (ord_ << 32) | (0xFFFFFFFF - row)
+    key ^= 1 << 63
+    return key - (1 << 64) if key >= 1 << 63 else key
+
+
+def top1_key_row(key) -> int:
+    """Global row of a (combined) top-1 key."""
+    return 0xFFFFFFFF - (int(key) & 0xFFFFFFFF)
 
 
 class GemvBatch:

@@ -220,7 +220,30 @@ int q4nx_gemv_top1(const q4nx_weight* w, const void* x_dev, int32_t* idx_dev, vo
   item.y = nullptr;
   item.TR = TR;
   item.TC = TC;
-  return from_cuda(launch_gemv_top1(w->kind, item, idx_dev, workspace_dev, info, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemv_top1(w->kind, item, idx_dev, nullptr, 0u, workspace_dev, info,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int q4nx_gemv_top1_key(const q4nx_weight* w, const void* x_dev, int64_t row_base, int64_t* key_dev,
+                       void* workspace_dev, uint64_t workspace_bytes, void* stream) {
+  int st = check_weight(w);
+  if (st) return st;
+  if (x_dev == nullptr || key_dev == nullptr) return Q4NX_E_NULL;
+  if (row_base < 0 || row_base > static_cast<int64_t>(INT32_MAX) - w->rows) return Q4NX_E_SHAPE;
+  if (!aligned16(x_dev) || (reinterpret_cast<uintptr_t>(key_dev) & 7u)) return Q4NX_E_ALIGN;
+  const int64_t TR = w->rows / 32, TC = w->cols / 256;
+  if (workspace_dev == nullptr || workspace_bytes < gemv_workspace_bytes(TR, TR * TC)) return Q4NX_E_WORKSPACE;
+  if (!aligned16(workspace_dev)) return Q4NX_E_ALIGN;
+  DeviceInfo info;
+  if (device_info(&info) != cudaSuccess) return Q4NX_E_CUDA;
+  GemvItem item;
+  item.chunks = w->chunks_dev;
+  item.x = x_dev;
+  item.y = nullptr;
+  item.TR = TR;
+  item.TC = TC;
+  return from_cuda(launch_gemv_top1(w->kind, item, nullptr, key_dev, static_cast<uint32_t>(row_base), workspace_dev,
+                                    info, static_cast<cudaStream_t>(stream)));
 }
 
 // Workspace of q4nx_gemm_m64: the GEMM's part (error word, posting counters,

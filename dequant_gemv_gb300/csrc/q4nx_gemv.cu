@@ -66,8 +66,11 @@ struct GemvArgsT {
   uint32_t* err;
   uint64_t* posted;        // [grid][MT][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
   // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
-  // row) key; the last CTA to finish writes the row index
-  int32_t* top1_idx;       // null: store y
+  // row) key; the last CTA to finish writes the row index and/or the key
+  int top1;                // 0: store y
+  uint32_t top1_row_base;  // added to the rows in the keys (a shard's first row)
+  int32_t* top1_idx;       // null, or where the row goes
+  int64_t* top1_key_out;   // null, or where the key goes (top bit flipped: signed order = key order)
   uint64_t* top1_key;      // workspace word, zero between launches
   uint32_t* top1_done;     // workspace word, zero between launches
 };
@@ -109,8 +112,8 @@ __device__ __forceinline__ void* token_y(const GemvArgs& a, void* y, int tok) {
 
 template <class GemvArgs>
 __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, float v) {
-  if (a.top1_idx) {
-    uint64_t key = argmax_key(v, static_cast<uint32_t>(n));
+  if (a.top1) {
+    uint64_t key = argmax_key(v, a.top1_row_base + static_cast<uint32_t>(n));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
     if ((threadIdx.x & 31) == 0) atomicMax(&s_top1_key, static_cast<unsigned long long>(key));
@@ -603,7 +606,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     for (int tok = 0; tok < MT; ++tok) v[tok] = finish_rows<KIND>(yacc[tok], lane, row);
     finish_segment<MT>(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
   }
-  if (MT == 1 && a.top1_idx) {
+  if (MT == 1 && a.top1) {
     // every warp's rows are folded in; the CTA's key goes to the launch's key,
     // and the last CTA to finish writes the index and clears the two words
     __syncthreads();
@@ -614,7 +617,8 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       if (atomicAdd(a.top1_done, 1u) == static_cast<uint32_t>(a.grid - 1)) {
         __threadfence();
         const unsigned long long best = atomicExch(reinterpret_cast<unsigned long long*>(a.top1_key), 0ull);
-        *a.top1_idx = argmax_index(best);
+        if (a.top1_idx) *a.top1_idx = argmax_index(best);
+        if (a.top1_key_out) *a.top1_key_out = static_cast<int64_t>(best ^ (1ull << 63));
         *a.top1_done = 0u;
       }
     }
@@ -727,9 +731,15 @@ static void fill_workspace(GemvArgsT<MAXB>& a, void* workspace) {
   a.posted = reinterpret_cast<uint64_t*>(ws + kWsErrBytes);
 }
 
+struct Top1Out {
+  int32_t* idx = nullptr;
+  int64_t* key = nullptr;
+  uint32_t row_base = 0;
+};
+
 template <int MAXB>
 static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
-                                     const DeviceInfo& info, int32_t* top1_idx, cudaStream_t s) {
+                                     const DeviceInfo& info, const Top1Out* top1, cudaStream_t s) {
   GemvArgsT<MAXB> a;
   fill_items(a, items, n);
   GemvPlan p;
@@ -741,7 +751,10 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   a.m = 1;
   a.x_stride = 0;
   a.y_stride = 0;
-  a.top1_idx = top1_idx;
+  a.top1 = top1 != nullptr;
+  a.top1_idx = top1 ? top1->idx : nullptr;
+  a.top1_key_out = top1 ? top1->key : nullptr;
+  a.top1_row_base = top1 ? top1->row_base : 0u;
   switch (kind) {
     case kQ4_1: return launch_gemv_t<kQ4_1, MAXB, 1>(a, p, s);
     case kQ4_K: return launch_gemv_t<kQ4_K, MAXB, 1>(a, p, s);
@@ -759,9 +772,13 @@ cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f3
   return launch_gemv_sized<kMaxBatch>(kind, items, n, out_f32, workspace, info, nullptr, s);
 }
 
-cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
-                             cudaStream_t s) {
-  return launch_gemv_sized<1>(kind, &item, 1, 1, workspace, info, idx, s);
+cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, int64_t* key, uint32_t row_base,
+                             void* workspace, const DeviceInfo& info, cudaStream_t s) {
+  Top1Out t;
+  t.idx = idx;
+  t.key = key;
+  t.row_base = row_base;
+  return launch_gemv_sized<1>(kind, &item, 1, 1, workspace, info, &t, s);
 }
 
 int gemv_max_tokens(int kind) {
@@ -790,7 +807,10 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
   a.m = M;
   a.x_stride = item.TC * 256 * 2;                 // X rows: cols bf16 each
   a.y_stride = item.TR * 32;                      // Y rows: rows elements each
+  a.top1 = 0;
   a.top1_idx = nullptr;
+  a.top1_key_out = nullptr;
+  a.top1_row_base = 0u;
   if (MT == 1) {                                  // one token: the single-GEMV kernel itself
     switch (kind) {
       case kQ4_1: return launch_gemv_t<kQ4_1, 1, 1>(a, p, s);

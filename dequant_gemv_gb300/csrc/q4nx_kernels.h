@@ -38,11 +38,13 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                               const DeviceInfo& info, cudaStream_t s);
 
-// GEMV of one item fused with top-1: *idx = the row of the largest fp32
-// output (ties: lowest row; a NaN output wins, the first one), y not written.
-// The workspace's bytes 4..15 hold the launch's top-1 words (zero between launches).
-cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, void* workspace, const DeviceInfo& info,
-                             cudaStream_t s);
+// GEMV of one item fused with top-1: the largest fp32 output (ties: lowest
+// row; a NaN output wins, the first one), y not written.  Writes the row to
+// *idx and/or the 64-bit key (top bit flipped, see q4nx.h) to *key, the rows
+// numbered from row_base.  The workspace's bytes 4..15 hold the launch's
+// top-1 words (zero between launches).
+cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, int64_t* key, uint32_t row_base,
+                             void* workspace, const DeviceInfo& info, cudaStream_t s);
 
 // ---- GEMV of one weight against M tokens (X [M][cols], Y [M][rows]) ----
 // Each chunk is read once for all M tokens.  M up to gemv_max_tokens(kind),

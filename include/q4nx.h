@@ -119,6 +119,24 @@ uint64_t q4nx_gemv_workspace(const q4nx_weight* w);
 int q4nx_gemv_top1(const q4nx_weight* w, const void* x_dev, int32_t* idx_dev, void* workspace_dev,
                    uint64_t workspace_bytes, void* stream);
 
+/* Vocabulary-sharded lm_head top-1 (the sharding of the lm_head rows over
+ * GPUs, each GPU holding a contiguous range of rows): the GEMV of this shard
+ * fused with top-1 as q4nx_gemv_top1 computes it, written as one 64-bit key
+ * instead of an index, so that the shards' winners combine with a single MAX
+ * reduction of int64 values (an all-reduce, or a max on the host):
+ *   key = (ord(v) << 32 | (0xFFFFFFFF - (row_base + n))) XOR (1 << 63)
+ * where v is the shard's largest fp32 output, n its row within the shard (the
+ * lowest of equal maxima; a NaN output counts as the largest, the first one
+ * winning) and ord maps fp32 to uint32 preserving order (-0 as +0, NaN to
+ * 0xFFFFFFFF).  The flipped top bit makes the signed int64 order equal the
+ * unsigned key order.  The global row of a combined key is
+ * 0xFFFFFFFF - (key & 0xFFFFFFFF).
+ * row_base: the shard's first global row, 0 <= row_base <= INT32_MAX - rows
+ * (Q4NX_E_SHAPE otherwise).  key_dev: device int64, 8-byte aligned.
+ * Workspace as for q4nx_gemv_top1. */
+int q4nx_gemv_top1_key(const q4nx_weight* w, const void* x_dev, int64_t row_base, int64_t* key_dev,
+                       void* workspace_dev, uint64_t workspace_bytes, void* stream);
+
 /* One GEMV of a batch: y_dev[rows] = w * x_dev[cols]. */
 typedef struct q4nx_gemv_item {
     q4nx_weight w;

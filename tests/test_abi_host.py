@@ -91,6 +91,12 @@ def test_validation_statuses(q):
     assert L.q4nx_gemv_top1(by(w), P, None, P, need, None) == 1
     assert L.q4nx_gemv_top1(by(w), P, P + 2, P, need, None) == 5
     assert L.q4nx_gemv_top1(by(w), P, P, P, need - 1, None) == 7
+    # sharded top-1 key: 8-byte aligned key, row base within int32 rows, workspace
+    assert L.q4nx_gemv_top1_key(by(w), P, 0, None, P, need, None) == 1
+    assert L.q4nx_gemv_top1_key(by(w), P, 0, P + 4, P, need, None) == 5
+    assert L.q4nx_gemv_top1_key(by(w), P, -1, P, P, need, None) == 3
+    assert L.q4nx_gemv_top1_key(by(w), P, 2**31 - 32, P, P, need, None) == 3
+    assert L.q4nx_gemv_top1_key(by(w), P, 0, P, P, need - 1, None) == 7
     assert L.q4nx_gemv_workspace(by(_w(q, rows=33))) == 0
     # gemv batch
     items = (q.q4nx_gemv_item * 3)()
