@@ -176,7 +176,9 @@ def run_reference(args, rank: int):
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": steps, "warmup": warm, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": "bounded per step"},
+            "config": {"workload": WORKLOAD, "layers": synth.QWEN3_06B_LAYERS, "matrices_per_step": len(mats),
+                       "weight_bytes_per_step": sum((n // 32) * (k // 256) * 5120 for _, _, n, k in mats),
+                       "kind": "q4_1", "batch": 1, "sample": "bounded per step"},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

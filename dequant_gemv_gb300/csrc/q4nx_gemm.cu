@@ -19,7 +19,7 @@
 // memory would spend two thirds of the SM's shared-memory bandwidth on A
 // alone, and the TMA fills, the code reads and the B reads need that bandwidth.
 //
-// Warp roles (24 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31 only):
+// Warp roles (16 warps; a warp reaches TMEM lanes 32*(warp%4) .. +31 only):
 //   warp 0       weight producer: per k-step the 4 chunks into one of the
 //                weight stages.  q4_1: the code regions (one 4-D tensor copy,
 //                128-byte swizzle, so that row-wise 16-byte reads are free of
@@ -44,8 +44,8 @@
 // sub-partition's issue slots with the dequant warps there, and fewer of them
 // let it keep the tensor pipe fed.
 // Two accumulators (2 x 64 TMEM columns) let the epilogue of one tile overlap
-// the main loop of the next.  A stage is filled by 17 arrivals (the X
-// producer's, with the TMA byte count, and the 16 dequant warps') and emptied
+// the main loop of the next.  A stage is filled by 9 arrivals (the X
+// producer's, with the TMA byte count, and the 8 dequant warps') and emptied
 // by one MMA commit, so the MMA thread waits once and commits once per k-step:
 // each wait or commit in that single issuing thread delays the tensor pipe.
 //
@@ -60,10 +60,12 @@
 // bounded; if one gives up, the CTA records the error in the workspace and
 // winds down.
 //
-// A CTA's last tile leaves through shared memory (the X stages are free once
-// its last MMA has completed): the epilogue warps stage the tile there and one
-// thread writes it with a single bulk copy (a TMA tensor store for Y, a 1-D
-// bulk store for a partial), instead of thousands of small scattered stores.
+// A CTA's last output tile leaves through shared memory (the X stages are
+// free once its last MMA has completed): the epilogue warps stage the tile
+// there and one thread writes it to Y with a single TMA tensor store, instead
+// of thousands of 64-byte stores.  Partials always go out from registers as
+// 512-byte coalesced stores, each warp then counting itself in with a release
+// reduction: the finisher waits on them, and this is the quickest way there.
 //
 // The finisher waits for CTAs of the same launch, so the launch relies on all
 // of its CTAs being resident at once: the grid is at most one CTA per SM, and
@@ -101,6 +103,18 @@ struct Plan {
   static_assert(kWBytes % 1024 == 0 && kXOff % 1024 == 0 && kXBytes % 1024 == 0, "swizzled regions 1024-aligned");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
+// Slots of shared memory for the last tile's later partials (32 KB each), free
+// once the CTA's last MMA has completed: three in the weight stages, two in X
+// stages 1 and 2 (X stage 0 stages the output tile).
+constexpr int kGatherSlots = 5;
+template <int KIND>
+__host__ __device__ constexpr int gather_slot(int i) {
+  return i < 3 ? kWOff + i * kXBytes : Plan<KIND>::kXOff + (i - 2) * kXBytes;
+}
+static_assert(3 * kXBytes <= Plan<kQ4_1>::kWStages * Plan<kQ4_1>::kWBytes, "three partials fit the q4_1 weight stages");
+static_assert(3 * kXBytes <= Plan<kQ8_KR>::kWStages * Plan<kQ8_KR>::kWBytes, "three partials fit the Q8 weight stages");
+static_assert(kStages == 3, "X stages 1 and 2 take two partials");
+
 constexpr int kDequantWarps = 8;                       // two per TMEM lane quarter, one half of the k-step each
 constexpr int kWarpW = 0, kWarpX = 1, kWarpMma = 2, kWarpAlloc = 3, kWarpDequant0 = 4;
 constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
@@ -235,15 +249,8 @@ __device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
 __device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ void sts_f32x4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 // shared -> global copies issued by one thread; `wait_written` returns once the
 // data is in global memory, `wait_read` once the shared source may be reused.
-__device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, uint32_t ssrc) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -251,7 +258,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_written() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
@@ -276,6 +282,7 @@ struct Shared {
   uint64_t acc_full[kAccs], acc_empty[kAccs];
   uint64_t drain;
   uint64_t staged;          // epilogue warps that have staged their rows of the last tile
+  uint64_t gather;          // the last tile's later partials, copied into free stage memory
   uint32_t tmem_base;
   volatile uint32_t abort_flag;
   uint32_t fix_seen;        // finisher's epilogue warps that have gathered every posted partial
@@ -435,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kAccs; ++s) { mbar_init(&sh->acc_full[s], 1); mbar_init(&sh->acc_empty[s], 4); }
     mbar_init(&sh->drain, 1);
     mbar_init(&sh->staged, 4);
+    mbar_init(&sh->gather, 1);
     sh->abort_flag = 0u;
     sh->fix_seen = 0u;
     fence_barrier_init();
@@ -583,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // finisher: the later CTAs' partials of this thread's row, summed in CTA
       // order, gathered before the accumulator is ready (token quad k in fx[k])
       float4 fx[kTileN / 4];
+      const bool last = t == ntiles - 1;
       if (finisher) {
         // each posting CTA counts once per epilogue warp
         const int64_t c_last = (u_hi * a.grid - 1) / a.units;
@@ -591,7 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4* p = reinterpret_cast<const float4*>(a.partials + (blockIdx.x + 1) * (kTileN * kTileM)) + row;
 #pragma unroll
         for (int k = 0; k < kTileN / 4; ++k) fx[k] = ld_cg_f32x4(p + k * kTileM);   // one round trip
-        for (int64_t c = blockIdx.x + 2; c <= c_last; ++c) {
+        // the later CTAs' partials: on the last tile, once the accumulator is
+        // final, through bulk copies into the then free stage memory (one
+        // round trip for all of them); beyond those slots, or on another tile,
+        // here, half a partial per round trip
+        for (int64_t c = blockIdx.x + 2 + (last ? kGatherSlots : 0); c <= c_last; ++c) {
           p = reinterpret_cast<const float4*>(a.partials + c * (kTileN * kTileM)) + row;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -614,36 +627,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid_row = n0 + row < a.N;
       float4* mine = reinterpret_cast<float4*>(a.partials + static_cast<int64_t>(blockIdx.x) * (kTileN * kTileM)) + row;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * e) << 16) + static_cast<uint32_t>(b * kTileN);
-      if (t == ntiles - 1) {
-        // last tile: stage it in X stage 0 ([16 quads][128 rows][4] fp32 for a
-        // partial, [64 tokens][128 rows] of the output type for Y), then one
-        // thread writes it out with a single bulk copy
+      if (last && !contrib) {
+        // last tile: stage it in X stage 0 ([64 tokens][128 rows] of the
+        // output type), then one thread writes it to Y with a single tensor
+        // copy.  (A partial goes out from registers below: its rows are
+        // 512-byte coalesced stores, and the finisher waits on it, so it
+        // should be visible as soon as possible.)
         const uint32_t stg = smem_u32(smem + kXOff);
+        if (finisher) {
+          const int64_t later = (u_hi * a.grid - 1) / a.units - blockIdx.x - 1;   // partials past the first
+          const int nsm = static_cast<int>(later < kGatherSlots ? later : kGatherSlots);
+          if (nsm > 0) {
+            if (warp == kWarpEpi0 && lane == 0) {
+              // the partials were seen through the counter's acquire; order that before the copies' reads
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              mbar_arrive_expect_tx(&sh->gather, static_cast<uint32_t>(nsm * kTileN * kTileM * 4));
+              for (int i = 0; i < nsm; ++i)
+                bulk_g2s(smem + gather_slot<KIND>(i), a.partials + (blockIdx.x + 2 + i) * (kTileN * kTileM),
+                         kTileN * kTileM * 4, &sh->gather);
+            }
+            if (!wait_bar(sh, &sh->gather, 0, a.err)) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+              for (int i = 0; i < nsm; ++i) {
+                const uint32_t src = smem_u32(smem + gather_slot<KIND>(i)) + static_cast<uint32_t>(row * 16);
+                float4 v[kTileN / 8];
+#pragma unroll
+                for (int k = 0; k < kTileN / 8; ++k) v[k] = lds_f32x4(src + static_cast<uint32_t>((8 * h + k) * kTileM * 16));
+#pragma unroll
+                for (int k = 0; k < kTileN / 8; ++k) {
+                  float4& f = fx[8 * h + k];
+                  f = make_float4(f.x + v[k].x, f.y + v[k].y, f.z + v[k].z, f.w + v[k].w);
+                }
+              }
+            }
+          }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float v[32];
           tmem_ld32(taddr + 32 * h, v);
-          if (contrib) {
+          if (finisher) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              sts_f32x4(stg + static_cast<uint32_t>(((8 * h + k) * kTileM + row) * 16), v[4 * k], v[4 * k + 1],
-                        v[4 * k + 2], v[4 * k + 3]);
-          } else {
-            if (finisher) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                v[4 * k] += fx[8 * h + k].x;
-                v[4 * k + 1] += fx[8 * h + k].y;
-                v[4 * k + 2] += fx[8 * h + k].z;
-                v[4 * k + 3] += fx[8 * h + k].w;
-              }
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] += fx[8 * h + k].x;
+              v[4 * k + 1] += fx[8 * h + k].y;
+              v[4 * k + 2] += fx[8 * h + k].z;
+              v[4 * k + 3] += fx[8 * h + k].w;
             }
+          }
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-              const uint32_t idx = static_cast<uint32_t>((32 * h + m) * kTileM + row);
-              if (a.out_f32) sts_f32(stg + idx * 4, v[m]);
-              else sts_u16(stg + idx * 2, f32_to_bf16_bits(v[m]));
-            }
+          for (int m = 0; m < 32; ++m) {
+            const uint32_t idx = static_cast<uint32_t>((32 * h + m) * kTileM + row);
+            if (a.out_f32) sts_f32(stg + idx * 4, v[m]);
+            else sts_u16(stg + idx * 2, f32_to_bf16_bits(v[m]));
           }
         }
         tc_fence_before();
@@ -655,17 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (warp == kWarpEpi0 && lane == 0) {
           if (!wait_bar(sh, &sh->staged, 0, a.err)) break;
-          if (contrib) {
-            bulk_s2g(a.partials + static_cast<int64_t>(blockIdx.x) * (kTileN * kTileM), stg, kTileN * kTileM * 4);
-            bulk_commit();
-            bulk_wait_written();
-            asm volatile("fence.proxy.async.global;" ::: "memory");     // the copy's writes before the count
-            red_release_add(&a.counters[tile], 4u);                     // all four epilogue warps' rows
-          } else {
-            tma_store_2d(&ymap, static_cast<int>(n0), 0, stg);
-            bulk_commit();
-            bulk_wait_read();
-          }
+          tma_store_2d(&ymap, static_cast<int>(n0), 0, stg);
+          bulk_commit();
+          bulk_wait_read();
         }
         continue;
       }
