@@ -3,6 +3,7 @@
 // Formulas: the "Q4NX chunks" section of the 1bit engine "NPU engine" page
 // (chunk-kind table; the decoders-and-repack paragraph below it).  Greedy
 // top-1: the page's "Serving" section (greedy decoding).
+#include <algorithm>
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
@@ -63,41 +64,87 @@ __global__ void __launch_bounds__(256) decode_q4_kernel(const uint8_t* __restric
   }
 }
 
-// Q8 kinds: the chunk's codes are column-oriented, so the CTA stages them in
-// shared memory; lane = row, and each thread emits 8 consecutive columns.
+// Q8 kinds: persistent CTAs, each walking the chunks c = blockIdx, +grid, ...
+// through a two-stage ring filled by 1-D bulk copies (the next chunk is on its
+// way while this one is decoded).  The codes are column-oriented, so a chunk
+// is decoded from shared memory with lane = row, each thread forming 8
+// consecutive columns; the decoded 32 x 256 tile is staged again in shared
+// memory (rows padded by 16 bytes, so that the 16-byte writes of a warp's 32
+// rows are free of bank conflicts) and leaves as one coalesced 512-byte store
+// per row.  Waits are bounded: a copy that never lands ends the CTA early.
+constexpr int kDecRowPitch = 512 + 16;
+constexpr int kDecStage = kQ8Bytes;
+constexpr int kDecQ8Smem = 2 * kDecStage + 32 * kDecRowPitch + 16;
+
+__device__ __forceinline__ void decode_q8_fetch(uint8_t* dst, const uint8_t* src, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, kQ8Bytes);
+  bulk_g2s(dst, src, kQ8Bytes, bar);
+}
+
 template <int KIND>
-__global__ void __launch_bounds__(256) decode_q8_kernel(const uint8_t* __restrict__ chunks, int64_t TC,
+__global__ void __launch_bounds__(256) decode_q8_kernel(const uint8_t* __restrict__ chunks, int64_t T, int64_t TC,
                                                         uint16_t* __restrict__ out) {
-  __shared__ __align__(16) uint8_t sc[kQ8Bytes];
-  const int64_t t = blockIdx.x;
-  const int64_t tr = t / TC, tc = t - tr * TC;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t* so = dsm + 2 * kDecStage;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(so + 32 * kDecRowPitch);
   const int64_t K = TC * 256;
-  const uint4* src = reinterpret_cast<const uint4*>(chunks + t * kQ8Bytes);
-  for (int i = threadIdx.x; i < kQ8Bytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(sc)[i] = __ldg(src + i);
+  const int64_t stride = gridDim.x;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_barrier_init();
+    for (int st = 0; st < 2; ++st) {
+      const int64_t c = blockIdx.x + st * stride;
+      if (c < T) decode_q8_fetch(dsm + st * kDecStage, chunks + c * kQ8Bytes, &bar[st]);
+    }
+  }
   __syncthreads();
   const int r = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int i = 0;
+  for (int64_t c = blockIdx.x; c < T; c += stride, ++i) {
+    const int st = i & 1;
+    if (!mbar_wait_bounded(&bar[st], (i >> 1) & 1)) break;
+    const uint8_t* sc = dsm + st * kDecStage;
+    const int64_t tr = c / TC, tc = c - tr * TC;
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int j = warp + 8 * jj;           // 8-column block 0..31
-    const int gidx = j >> 2;
-    const float d = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(sc + kQ8D)[r * 8 + gidx]);
-    uint32_t o[4];
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = warp + 8 * jj;           // 8-column block 0..31
+      const int gidx = j >> 2;
+      const float d = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(sc + kQ8D)[r * 8 + gidx]);
+      uint32_t o[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      float wv[2];
+      for (int p = 0; p < 4; ++p) {
+        float wv[2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int k = 8 * j + 2 * p + e;
-        int off;
-        if constexpr (KIND == kQ8_KR) off = k * 32 + r;
-        else off = (r >> 4) * 4096 + (k >> 5) * 512 + (k & 31) * 16 + (r & 15);
-        wv[e] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc[off])));
+        for (int e = 0; e < 2; ++e) {
+          const int k = 8 * j + 2 * p + e;
+          int off;
+          if constexpr (KIND == kQ8_KR) off = k * 32 + r;
+          else off = (r >> 4) * 4096 + (k >> 5) * 512 + (k & 31) * 16 + (r & 15);
+          wv[e] = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc[off])));
+        }
+        o[p] = static_cast<uint32_t>(f32_to_bf16_bits(wv[0])) | (static_cast<uint32_t>(f32_to_bf16_bits(wv[1])) << 16);
       }
-      o[p] = static_cast<uint32_t>(f32_to_bf16_bits(wv[0])) | (static_cast<uint32_t>(f32_to_bf16_bits(wv[1])) << 16);
+      *reinterpret_cast<uint4*>(so + r * kDecRowPitch + j * 16) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint16_t* dst = out + (tr * 32 + r) * K + tc * 256 + j * 8;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    __syncthreads();                         // the stage is read out and the tile is staged
+    if (threadIdx.x == 0 && c + 2 * stride < T)
+      decode_q8_fetch(dsm + st * kDecStage, chunks + (c + 2 * stride) * kQ8Bytes, &bar[st]);
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = warp * 4 + q;
+      uint16_t* dst = out + (tr * 32 + row) * K + tc * 256 + lane * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(so + row * kDecRowPitch + lane * 16);
+    }
+    __syncthreads();                         // the staged tile is written out before the next one
   }
+  // a CTA that stopped early lets its copies in flight land before it exits
+  if (threadIdx.x == 0)
+    for (int k = 0; k < 2; ++k) {
+      const int64_t c = blockIdx.x + static_cast<int64_t>(i + k) * stride;
+      if (c < T) mbar_wait_bounded(&bar[(i + k) & 1], ((i + k) >> 1) & 1);
+    }
 }
 
 cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, void* out, cudaStream_t s) {
@@ -109,8 +156,24 @@ cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, 
   switch (kind) {
     case kQ4_1: decode_q4_kernel<kQ4_1><<<grid, 256, 0, s>>>(c, TC, o); break;
     case kQ4_K: decode_q4_kernel<kQ4_K><<<grid, 256, 0, s>>>(c, TC, o); break;
-    case kQ8_KR: decode_q8_kernel<kQ8_KR><<<grid, 256, 0, s>>>(c, TC, o); break;
-    case kQ8_BLK: decode_q8_kernel<kQ8_BLK><<<grid, 256, 0, s>>>(c, TC, o); break;
+    case kQ8_KR:
+    case kQ8_BLK: {
+      // persistent: as many CTAs as fit on the GPU at once, never more than chunks
+      const void* f = kind == kQ8_KR ? reinterpret_cast<const void*>(decode_q8_kernel<kQ8_KR>)
+                                     : reinterpret_cast<const void*>(decode_q8_kernel<kQ8_BLK>);
+      cudaError_t e = set_max_dynamic_smem(f, kind == kQ8_KR ? 29 : 30);
+      if (e != cudaSuccess) return e;
+      int dev = 0, sms = 0, per_sm = 0;
+      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, 256, kDecQ8Smem)) != cudaSuccess) return e;
+      const int64_t g = std::min<int64_t>(T, static_cast<int64_t>(sms) * std::max(per_sm, 1));
+      if (kind == kQ8_KR)
+        decode_q8_kernel<kQ8_KR><<<static_cast<unsigned>(g), 256, kDecQ8Smem, s>>>(c, T, TC, o);
+      else
+        decode_q8_kernel<kQ8_BLK><<<static_cast<unsigned>(g), 256, kDecQ8Smem, s>>>(c, T, TC, o);
+      break;
+    }
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
