@@ -496,7 +496,7 @@ def run_suite(args):
                 emit({"suite": "pack_q4_1", "workload": f"{sname} {N}x{K} -> q4_1", "us": us,
                       "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
                 del srcs
-        if wid in (1, 5) and want("decode"):
+        if wid in (1, 3, 4, 5) and want("decode"):
             outs = [torch.empty((N, K), dtype=torch.bfloat16, device=dev) for _ in range(min(R, 2))]
             us = timeit([lambda W=W, o=outs[i % len(outs)]: q.q4nx_decode(W, out=o) for i, W in enumerate(Ws)], 64)
             alg = nb + 2 * N * K
