@@ -646,11 +646,11 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
   // dependent launch) starts its weight copies on the same SMs while this one
   // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
   // chunks are larger and gain more from a deeper ring than from that overlap.
-  // (less 64 bytes for the kernel's static shared memory)
+  // (less 256 bytes for the kernel's static shared memory, 128 bytes today)
   // Several tokens need more registers than two CTAs per SM leave, so those
   // launches take the whole of the shared memory.
   const uint64_t cap =
-      static_cast<uint64_t>(CB <= kQ41Bytes && MT == 1 ? info.smem_two_per_sm : info.max_smem_optin) - 64;
+      static_cast<uint64_t>(CB <= kQ41Bytes && MT == 1 ? info.smem_two_per_sm : info.max_smem_optin) - 256;
   const int max_warps = gemv_max_warps(kind, MT);
   static const int kWarpChoices[] = {12, 8, 6, 4, 2, 1};
   int warps = 0, stages = 0;
