@@ -383,9 +383,11 @@ __device__ __forceinline__ void dequant_half(uint32_t codes, uint32_t scales, in
 // lanes read 32 rows of one column together.  Plain C++ loads: they stay
 // behind the stage's barrier wait (an asm statement with a memory clobber).
 template <int KIND>
-__device__ __forceinline__ void dequant_half_q8(const uint8_t* chunk, int r, int qh, uint32_t (&out)[64]) {
-  const uint2 dw = *reinterpret_cast<const uint2*>(chunk + kQ8D + r * 16 + qh * 8);   // d of groups 4qh .. 4qh+3
-  const uint8_t* c = chunk + (KIND == kQ8_KR ? r + qh * (128 * 32) : (r >> 4) * 4096 + (r & 15) + qh * (4 * 512));
+// (shared-memory loads by explicit .shared address: a generic pointer would
+// take the slower generic path for each of the 128 byte loads)
+__device__ __forceinline__ void dequant_half_q8(uint32_t chunk, int r, int qh, uint32_t (&out)[64]) {
+  const uint2 dw = lds64(chunk + kQ8D + r * 16 + qh * 8);   // d of groups 4qh .. 4qh+3
+  const uint32_t c = chunk + (KIND == kQ8_KR ? r + qh * (128 * 32) : (r >> 4) * 4096 + (r & 15) + qh * (4 * 512));
   const float2 kBias = make_float2(-8388736.f, -8388736.f);   // 2^23 + 128
 #pragma unroll
   for (int gg = 0; gg < 4; ++gg) {
@@ -397,7 +399,7 @@ __device__ __forceinline__ void dequant_half_q8(const uint8_t* chunk, int r, int
       const int k = 32 * gg + 2 * p;                // column within the half
       const int o0 = KIND == kQ8_KR ? k * 32 : (k >> 5) * 512 + (k & 31) * 16;
       const int o1 = KIND == kQ8_KR ? (k + 1) * 32 : ((k + 1) >> 5) * 512 + ((k + 1) & 31) * 16;
-      const uint32_t u0 = c[o0], u1 = c[o1];
+      const uint32_t u0 = lds_u8(c + o0), u1 = lds_u8(c + o1);
       // int8 code -> exact fp32: the bits 0x4B000000 | (u ^ 0x80) are 2^23 + 128 + code
       const float2 f = make_float2(__uint_as_float((u0 ^ 0x80u) | 0x4B000000u), __uint_as_float((u1 ^ 0x80u) | 0x4B000000u));
       const float2 w = __fmul2_rn(fadd2(f, kBias), d2);
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (the last tile may hold fewer than 4 tile rows: the rows past the end
       // decode whatever the stage holds, and their results are never stored)
       if constexpr (P::kQ8) {
-        dequant_half_q8<KIND>(smem + kWOff + ws * kWBytes + i * kQ8Bytes, lane, qh, out);
+        dequant_half_q8<KIND>(smem_u32(smem + kWOff + ws * kWBytes + i * kQ8Bytes), lane, qh, out);
       } else {
         const uint32_t wst = smem_u32(smem + kWOff + ws * kWBytes);
         dequant_half(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qh, out);
