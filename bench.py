@@ -511,8 +511,8 @@ def run_suite(args):
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
         small_ms = {synth.Q4_1: (2, 3, 4, 8, 16), synth.Q4_K: (2, 4), synth.Q8_KR: (2, 4), synth.Q8_BLK: (2,)}
         if ((kind == synth.Q4_1 and wid == 4) or kind == synth.Q4_K or wid == 5) and want("gemm_small_m"):
-            # small token blocks (verify windows, multi-token prediction): two tokens (Q4_K: up
-            # to four) on the CUDA cores, more on the tensor cores
+            # small token blocks (verify windows, multi-token prediction): q4_1 two tokens and
+            # Q4_K up to four on the CUDA cores, more (and Q8 from two) on the tensor cores
             for M in small_ms[kind]:
                 X = dev_bf16(synth.workload_activations(wid, 0, M, K))
                 Y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
@@ -521,7 +521,7 @@ def run_suite(args):
                                       device=dev)
                 us = timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, out_dtype=od, ws=gws) for W in Ws], 400)
                 alg = nb + 2 * M * K + (4 if out_f32 else 2) * M * N
-                cores = "cuda" if M <= (4 if kind == synth.Q4_K else 2) else "tensor"
+                cores = "cuda" if M <= {synth.Q4_1: 2, synth.Q4_K: 4}.get(kind, 1) else "tensor"
                 emit({"suite": "gemm_small_m", "workload": name, "M": M, "path": cores, "us": us,
                       "weight_gbs": nb / us / 1e3,
                       "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})

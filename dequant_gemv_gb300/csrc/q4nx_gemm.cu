@@ -140,6 +140,7 @@ struct Args {
   float* partials;          // [grid][16 token quads][128 rows][4]: at most one partial per CTA
   int64_t TR, TC, N;
   int tiles, M, out_f32, grid;
+  int mrows;                // X box rows: M rounded up to 8
   int64_t units;            // tiles * TC
 };
 
@@ -172,12 +173,21 @@ __device__ __forceinline__ void issue_weights_q8(uint32_t dst, const CUtensorMap
 }
 // One k-step of X, on one elected lane: arm `bar` for 32 KB, then copy
 // X[0:64, 256 ks .. +255] as 4 boxes of 64 tokens x 64 k (128-byte swizzle).
-__device__ __forceinline__ void issue_x(uint32_t dst, const CUtensorMap* xmap, int ks, uint32_t bar) {
+// X of one k-step: four boxes of 64 columns x mrows tokens (M rounded up to 8,
+// so that a box reaches at most 7 token rows past the end of X: boxes mostly
+// outside the tensor are slow to fill), each into its 8 KB slot of the stage.
+// Rows from mrows to 63 of a slot keep whatever they held: they only reach
+// accumulator columns of tokens that are never stored.
+__device__ __forceinline__ void issue_x(uint32_t dst, const CUtensorMap* xmap, int ks, uint32_t bar, int mrows) {
   asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "{\n\t.reg .pred e;\n\t.reg .b32 x1, x2, x3;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "add.u32 x1, %2, 64;\n\tadd.u32 x2, %2, 128;\n\tadd.u32 x3, %2, 192;\n\t"
       "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
-      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {0, 0, %2}], [%3];\n\t}"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(xmap)), "r"(4 * ks), "r"(bar), "n"(4 * 64 * 128)
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, 0}], [%3];\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0+8192], [%1, {x1, 0}], [%3];\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0+16384], [%1, {x2, 0}], [%3];\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0+24576], [%1, {x3, 0}], [%3];\n\t}"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(xmap)), "r"(256 * ks), "r"(bar), "r"(4 * 128 * mrows)
       : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -389,6 +399,7 @@ __device__ __forceinline__ void dequant_half_q8(uint32_t chunk, int r, int qh, u
   const uint2 dw = lds64(chunk + kQ8D + r * 16 + qh * 8);   // d of groups 4qh .. 4qh+3
   const uint32_t c = chunk + (KIND == kQ8_KR ? r + qh * (128 * 32) : (r >> 4) * 4096 + (r & 15) + qh * (4 * 512));
   const float2 kBias = make_float2(-8388736.f, -8388736.f);   // 2^23 + 128
+  const uint32_t hi16 = KIND == kQ8_BLK && r >= 16 ? 16u : 0u;  // BLK: the 16-byte stagger of the upper half-warp
 #pragma unroll
   for (int gg = 0; gg < 4; ++gg) {
     const uint32_t dp = gg < 2 ? dw.x : dw.y;
@@ -399,7 +410,18 @@ __device__ __forceinline__ void dequant_half_q8(uint32_t chunk, int r, int qh, u
       const int k = 32 * gg + 2 * p;                // column within the half
       const int o0 = KIND == kQ8_KR ? k * 32 : (k >> 5) * 512 + (k & 31) * 16;
       const int o1 = KIND == kQ8_KR ? (k + 1) * 32 : ((k + 1) >> 5) * 512 + ((k + 1) & 31) * 16;
-      const uint32_t u0 = lds_u8(c + o0), u1 = lds_u8(c + o1);
+      uint32_t u0, u1;
+      if constexpr (KIND == kQ8_KR) {
+        u0 = lds_u8(c + o0);
+        u1 = lds_u8(c + o1);
+      } else {
+        // BLK keeps rows 16-31 4096 bytes after rows 0-15, on the same banks:
+        // the upper half-warp reads the pair's other column first (16 bytes
+        // on), so that each load meets 8 distinct banks, and swaps back
+        const uint32_t ua = lds_u8(c + o0 + hi16), ub = lds_u8(c + o1 - hi16);
+        u0 = hi16 ? ub : ua;
+        u1 = hi16 ? ua : ub;
+      }
       // int8 code -> exact fp32: the bits 0x4B000000 | (u ^ 0x80) are 2^23 + 128 + code
       const float2 f = make_float2(__uint_as_float((u0 ^ 0x80u) | 0x4B000000u), __uint_as_float((u1 ^ 0x80u) | 0x4B000000u));
       const float2 w = __fmul2_rn(fadd2(f, kBias), d2);
@@ -485,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; j < n; ++j) {
       const int s = j % kStages;
       if (!wait_bar_warp(sh, &sh->empty[s], ((j / kStages) & 1) ^ 1u, a.err)) break;
-      issue_x(smem_u32(smem + kXOff + s * kXBytes), &xmap, static_cast<int>(ks), smem_u32(&sh->full[s]));
+      issue_x(smem_u32(smem + kXOff + s * kXBytes), &xmap, static_cast<int>(ks), smem_u32(&sh->full[s]), a.mrows);
       if (++ks == KS) ks = 0;
     }
     // copies still in flight land first (a stage whose dequant part stopped short stays incomplete:
@@ -821,11 +843,12 @@ cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void
     }
   }
   {
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(TC * 4)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(TC * 256 * 2), 128};
-    cuuint32_t box[3] = {64, 64, 4};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(X), dims, strides, box, es,
+    // X [M][K]: boxes of 64 columns x mrows tokens
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(TC * 256), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(TC * 256 * 2)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>((M + 7) & ~7)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -854,6 +877,7 @@ cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void
   a.N = TR * 32;
   a.tiles = static_cast<int>(tiles);
   a.M = M;
+  a.mrows = (M + 7) & ~7;
   a.out_f32 = out_f32;
   a.units = tiles * TC;
   // at least 4 k-steps per CTA where the work allows it, at most one CTA per SM

@@ -824,8 +824,6 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
     switch (kind) {
       case kQ4_1: return launch_gemv_t<kQ4_1, 1, 2>(a, p, s);
       case kQ4_K: return launch_gemv_t<kQ4_K, 1, 2>(a, p, s);
-      case kQ8_KR: return launch_gemv_t<kQ8_KR, 1, 2>(a, p, s);
-      case kQ8_BLK: return launch_gemv_t<kQ8_BLK, 1, 2>(a, p, s);
       default: return cudaErrorInvalidValue;
     }
   }

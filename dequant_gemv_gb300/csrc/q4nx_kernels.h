@@ -49,10 +49,11 @@ cudaError_t launch_gemv_top1(int kind, const GemvItem& item, int32_t* idx, int64
 // ---- GEMV of one weight against M tokens (X [M][cols], Y [M][rows]) ----
 // Each chunk is read once for all M tokens.  M up to gemv_max_tokens(kind),
 // the M up to which this beats the tensor-core GEMM on GB300 (measured: two
-// tokens for q4_1 and Q8); Q4_K has no tensor-core path, so it goes to four.
-// `workspace`: gemv_workspace_bytes(.., .., 4) bytes, zero-filled and left
-// so; `err`: the error word to report a failed wait in.
-constexpr int kGemvTokensQ41 = 2, kGemvTokensQ4K = 4, kGemvTokensQ8 = 2, kGemvTokensMax = 4;
+// tokens for q4_1, one for Q8, whose float path costs more per token); Q4_K
+// has no tensor-core path, so it goes to four.  `workspace`:
+// gemv_workspace_bytes(.., .., 4) bytes, zero-filled and left so; `err`: the
+// error word to report a failed wait in.
+constexpr int kGemvTokensQ41 = 2, kGemvTokensQ4K = 4, kGemvTokensQ8 = 1, kGemvTokensMax = 4;
 int gemv_max_tokens(int kind);
 cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f32, uint32_t* err, void* workspace,
                                const DeviceInfo& info, cudaStream_t s);

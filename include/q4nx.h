@@ -159,9 +159,9 @@ uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
 /* Fused decode + GEMM for a block of 1..64 tokens on the tcgen05 tensor cores:
  *   Y[m][n] = sum_k X[m][k] * w[n][k],  m < M.
  * X_dev: bf16 [M][cols] row-major.  Y_dev: [M][rows] row-major of out_dtype.
- * A few tokens (M <= 2, or M <= 4 for Q4_K) run on the CUDA cores: each chunk
- * is read once and its codes enter exact integer (4-bit) or fp32 (Q8) dot
- * products with every token, as in q4nx_gemv (M = 1 is q4nx_gemv's kernel).  Larger M runs on
+ * A few tokens run on the CUDA cores (M = 1 for every kind, as q4nx_gemv;
+ * M = 2 for q4_1; M <= 4 for Q4_K): each chunk is read once and its codes
+ * enter exact integer dot products with every token.  Larger M runs on
  * the tensor cores: weights are decoded to bf16 (code*scale + zero for q4_1,
  * rounded once; d*code for Q8, exactly the standalone decode) into tensor
  * memory and multiplied with fp32 accumulation there; kinds q4_1, Q8_KR,

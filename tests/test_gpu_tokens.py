@@ -1,7 +1,8 @@
-"""q4nx_gemm_m64 for a few tokens: M <= 2 (M <= 4 for Q4_K) run on the CUDA
-cores, each chunk read once and entering the dot products of every token with
-the per-token arithmetic of q4nx_gemv; q4_1 and Q8 at M = 3, 4 take the
-tensor-core path, checked here to the same bar.
+"""q4nx_gemm_m64 for a few tokens: q4_1 at M <= 2 and Q4_K at M <= 4 run on
+the CUDA cores, each chunk read once and entering the dot products of every
+token with the per-token arithmetic of q4nx_gemv (M = 1: q4nx_gemv's kernel
+for every kind); the other cases take the tensor-core path, checked here to
+the same bar.
 
 Checks: every output within the bar of the other GPU tests against the binary64
 oracle; a repeated call bit-identical (partials are added in a fixed order);
