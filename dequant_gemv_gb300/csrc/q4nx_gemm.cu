@@ -400,6 +400,7 @@ __device__ __forceinline__ void dequant_half_q8(uint32_t chunk, int r, int qh, u
   const uint32_t c = chunk + (KIND == kQ8_KR ? r + qh * (128 * 32) : (r >> 4) * 4096 + (r & 15) + qh * (4 * 512));
   const float2 kBias = make_float2(-8388736.f, -8388736.f);   // 2^23 + 128
   const uint32_t hi16 = KIND == kQ8_BLK && r >= 16 ? 16u : 0u;  // BLK: the 16-byte stagger of the upper half-warp
+  const uint32_t swap_sel = hi16 ? 0x1032u : 0x3210u;          // ... and the swap of its bf16 halves
 #pragma unroll
   for (int gg = 0; gg < 4; ++gg) {
     const uint32_t dp = gg < 2 ? dw.x : dw.y;
@@ -410,22 +411,19 @@ __device__ __forceinline__ void dequant_half_q8(uint32_t chunk, int r, int qh, u
       const int k = 32 * gg + 2 * p;                // column within the half
       const int o0 = KIND == kQ8_KR ? k * 32 : (k >> 5) * 512 + (k & 31) * 16;
       const int o1 = KIND == kQ8_KR ? (k + 1) * 32 : ((k + 1) >> 5) * 512 + ((k + 1) & 31) * 16;
-      uint32_t u0, u1;
-      if constexpr (KIND == kQ8_KR) {
-        u0 = lds_u8(c + o0);
-        u1 = lds_u8(c + o1);
-      } else {
-        // BLK keeps rows 16-31 4096 bytes after rows 0-15, on the same banks:
-        // the upper half-warp reads the pair's other column first (16 bytes
-        // on), so that each load meets 8 distinct banks, and swaps back
-        const uint32_t ua = lds_u8(c + o0 + hi16), ub = lds_u8(c + o1 - hi16);
-        u0 = hi16 ? ub : ua;
-        u1 = hi16 ? ua : ub;
-      }
+      // BLK keeps rows 16-31 4096 bytes after rows 0-15, on the same banks:
+      // the upper half-warp reads the pair's other column first (16 bytes
+      // on), so that each load meets 8 distinct banks, and swaps the two
+      // bf16 halves of its result back
+      const uint32_t u0 = lds_u8(c + o0 + hi16), u1 = lds_u8(c + o1 - hi16);
       // int8 code -> exact fp32: the bits 0x4B000000 | (u ^ 0x80) are 2^23 + 128 + code
       const float2 f = make_float2(__uint_as_float((u0 ^ 0x80u) | 0x4B000000u), __uint_as_float((u1 ^ 0x80u) | 0x4B000000u));
       const float2 w = __fmul2_rn(fadd2(f, kBias), d2);
-      out[16 * gg + p] = pack_bf16x2(w.x, w.y);
+      if constexpr (KIND == kQ8_KR) {
+        out[16 * gg + p] = pack_bf16x2(w.x, w.y);
+      } else {
+        out[16 * gg + p] = prmt(pack_bf16x2(w.x, w.y), 0u, swap_sel);
+      }
     }
   }
 }
