@@ -373,6 +373,7 @@ def run_gpu(args, rank: int, world: int):
                        "l2": "inputs larger than L2 (275 MB of weights streamed per step)",
                        "launch": "one q4nx_gemv_batch launch of all 196 matrices per step; CUDA graphs of "
                                  f"{per_graph} consecutive steps, replayed back to back",
+                       "us_per_layer": ms_per_step * 1e3 / synth.QWEN3_06B_LAYERS,
                        "other_schedules": alt,
                        "hbm_frac_of_nominal_8tbs": value / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
