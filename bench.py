@@ -451,6 +451,7 @@ def run_suite(args):
         (4, "q4_1 4096x12288", synth.Q4_1, 4096, 12288),
         (5, "Q8 KR 151936x2560", synth.Q8_KR, 151936, 2560),
         (5, "Q8 BLK 151936x2560", synth.Q8_BLK, 151936, 2560),
+        (6, "q4_1 151936x2560", synth.Q4_1, 151936, 2560),     # an lm_head-sized q4_1 matrix (243 MB)
     ]
     only = set(args.only.split(",")) if args.only else None
     want = lambda k: only is None or k in only
@@ -475,7 +476,7 @@ def run_suite(args):
             emit({"suite": "gemv", "workload": name, "M": 1, "us": us, "weight_gbs": nb / us / 1e3,
                   "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm},
                   "frac_of_nominal_8tbs": nb / us / 1e3 / 8000.0, "copies": R})
-        if wid == 5 and want("top1"):
+        if wid in (5, 6) and want("top1"):
             # lm_head GEMV fused with top-1 (logits never written) vs the GEMV then the argmax kernel
             idx1 = torch.empty(1, dtype=torch.int32, device=dev)
             yl = torch.empty((1, N), dtype=torch.float32, device=dev)
@@ -526,7 +527,7 @@ def run_suite(args):
                 emit({"suite": "gemm_small_m", "workload": name, "M": M, "path": cores, "us": us,
                       "weight_gbs": nb / us / 1e3,
                       "roofline": {"bound": "hbm", "achieved": alg / us / 1e3, "peak": hbm, "frac": alg / us / 1e3 / hbm}})
-        if ((kind == synth.Q4_1 and wid == 4) or wid == 5) and want("gemm_m64"):
+        if ((kind == synth.Q4_1 and wid in (4, 6)) or wid == 5) and want("gemm_m64"):
             M = 64
             X = dev_bf16(synth.workload_activations(wid, 0, M, K))
             Y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)

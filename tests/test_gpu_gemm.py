@@ -120,6 +120,14 @@ def test_gemm_q8_lm_head_64_tokens(q, kind):
     run(q, kind, N, K, 64, out="f32", rows=rows, wid=5)
 
 
+def test_gemm_q4_1_lm_head_64_tokens(q):
+    """An lm_head-sized q4_1 matrix (151936x2560, 243 MB) at 64 tokens, bf16 out (rows sampled)."""
+    N, K = 151936, 2560
+    rows = np.unique(np.concatenate([np.arange(0, 160), np.arange(N - 160, N),
+                                     np.random.default_rng(6).integers(0, N, 600)]))
+    run(q, synth.Q4_1, N, K, 64, out="bf16", rows=rows, wid=6)
+
+
 def test_gemm_q8_layouts_agree_on_the_same_weights(q):
     """The same logical codes packed in layout KR and in layout BLK give the same products, bit for bit."""
     N, K, M = 512, 2048, 64

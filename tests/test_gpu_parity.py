@@ -152,6 +152,7 @@ def test_gemv_small(q, kind, N, K, out):
     (synth.Q4_K, 9728, 2560, 3, "bf16"), (synth.Q4_K, 2560, 9728, 3, "bf16"),
     (synth.Q4_1, 12288, 4096, 4, "bf16"), (synth.Q4_1, 4096, 12288, 4, "bf16"),
     (synth.Q8_KR, 151936, 2560, 5, "f32"), (synth.Q8_BLK, 151936, 2560, 5, "f32"),
+    (synth.Q4_1, 151936, 2560, 6, "f32"),
 ])
 def test_gemv_workload_sizes(q, kind, N, K, wid, out):
     f, w = synth.make(kind, N, K, synth.rng(wid, 0, 0))
