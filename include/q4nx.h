@@ -170,6 +170,9 @@ uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
  * expects its CTAs (at most one per SM) to be resident together, as they are
  * when no other kernel occupies the GPU; a stalled launch gives up after a
  * bounded wait and reports it through q4nx_check.
+ * Accuracy: CUDA-core outputs as q4nx_gemv; tensor-core outputs multiply
+ * bf16-rounded weights, each within 2^-9 of itself, so an output may differ
+ * from the exact sum by that much of sum_k |w x| beyond the fp32 rounding.
  * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes (the same for every
  * M), zero-filled before first use; it holds the error word, and calls may
  * leave partial sums in it, so it is not shared with the GEMV entry points. */
