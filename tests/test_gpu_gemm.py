@@ -1,9 +1,11 @@
 """Parity of the tensor-core decode + GEMM (q4nx_gemm_m64) with the oracle, for
 q4_1 chunks and Q8 chunks in both code layouts.
 
-Bar: every output within 1e-3 * sum_k |w_k x_k| of the binary64 oracle, plus
-2^-9 * sum_k |w_k x_k| for the bf16 rounding of the weights the tensor cores
-multiply (reading o21) and 2^-8 |y| for bf16 outputs; per-row cosine >= 0.99999.  The kernel multiplies
+Bar: every output within 1e-3 * sum_k |w_k x_k| of the binary64 oracle (plus
+2^-8 |y| for bf16 outputs), per-row cosine >= 0.99999.  Shapes narrower than
+the configurations (K < 2560) add 2^-9 * sum_k |w_k x_k| for the bf16 rounding
+of the weights the tensor cores multiply (reading o21), which short sums do
+not average out.  The kernel multiplies
 bf16-decoded weights with fp32 accumulation on tcgen05 tensor cores.
 """
 import dataclasses
@@ -37,7 +39,10 @@ def run(q, kind, N, K, M, out="f32", rows=None, seed=0, wid=4):
     Y = out_values(q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype=out))
     assert Y.shape == (M, N)
     Y64, A = oracle.matmul(w, kind, N, K, X, rows=rows)
-    assert_within(Y if rows is None else Y[:, rows], Y64, A, out == "bf16", f"gemm {N}x{K} M={M}", bf16_weights=True)
+    # the configurations' widths (K >= 2560) meet the plain 1e-3 bar: over long
+    # sums the weights' bf16 rounding averages out; short ones take reading o21
+    assert_within(Y if rows is None else Y[:, rows], Y64, A, out == "bf16", f"gemm {N}x{K} M={M}",
+                  bf16_weights=K < 2560)
     return Y
 
 

@@ -61,7 +61,7 @@ def test_tokens_match_oracle(q, kind, N, K, M, out):
     Y64, A = oracle.matmul(w, kind, N, K, X, rows=rows)
     # (q4_1 and Q8 at larger M take the tensor-core path: bf16 weights, reading o21)
     assert_within(got if rows is None else got[:, rows], Y64, A, out == "bf16", f"tokens kind {kind} {N}x{K} M={M}",
-                  bf16_weights=tensor_path(kind, M))
+                  bf16_weights=tensor_path(kind, M) and K < 2560)
     again = q.q4nx_gemm_m64(W, Xd, out_dtype=out)
     bits = torch.int16 if out == "bf16" else torch.int32
     assert torch.equal(Y.view(bits), again.view(bits)), "a repeated call gave different bits"
