@@ -39,7 +39,7 @@ def _case(q, kind, N, K, M, seed):
     return w, X, q.Weight(to_dev_bytes(w), kind, N, K), to_dev_bf16(X)
 
 
-SHAPES = [(96, 768), (160, 2816), (1024, 1024), (4096, 4096)]
+SHAPES = [(32, 256), (2080, 256), (96, 768), (160, 2816), (1024, 1024), (4096, 4096)]
 
 
 def tensor_path(kind, M):
