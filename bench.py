@@ -449,6 +449,9 @@ def run_suite(args):
         (3, "Q4_K 2560x9728", synth.Q4_K, 2560, 9728),
         (4, "q4_1 12288x4096", synth.Q4_1, 12288, 4096),
         (4, "q4_1 4096x12288", synth.Q4_1, 4096, 12288),
+        # gate and up of the same block as one weight: their chunk arrays concatenated (tile rows of
+        # gate, then of up), one launch for both since they read the same activations
+        (4, "q4_1 24576x4096", synth.Q4_1, 24576, 4096),
         (5, "Q8 KR 151936x2560", synth.Q8_KR, 151936, 2560),
         (5, "Q8 BLK 151936x2560", synth.Q8_BLK, 151936, 2560),
         (6, "q4_1 151936x2560", synth.Q4_1, 151936, 2560),     # an lm_head-sized q4_1 matrix (243 MB)
@@ -553,6 +556,55 @@ def run_suite(args):
                                    "frac": 4 * M * N / us / 1e3 / hbm}})
         del Ws, base
         torch.cuda.empty_cache()
+    if want("block") and (not args.case or args.case in "prefill block"):
+        run_block(args, q, dev, stream, timeit, emit, dev_bytes, dev_bf16, copies_for, hbm, tc_peak)
+
+
+def run_block(args, q, dev, stream, timeit, emit, dev_bytes, dev_bf16, copies_for, hbm, tc_peak):
+    """The 8B-width MLP block as a sequence: gate|up (24576x4096, one merged
+    weight) then down (4096x12288), at M = 1 (GEMV) and M = 64 (tensor cores),
+    each launch reading the weights of another copy, so the timed sequence
+    streams every weight byte from HBM."""
+    import torch
+
+    shapes = [(24576, 4096), (4096, 12288)]
+    mats = []
+    for i, (N, K) in enumerate(shapes):
+        f, w = synth.make(synth.Q4_1, N, K, synth.rng(4, 10 + i, 0))
+        base = dev_bytes(w)
+        R = copies_for(w.size)
+        mats.append((N, K, w.size, [q.Weight(base if r == 0 else base.clone(), synth.Q4_1, N, K) for r in range(R)]))
+    R = min(len(m[3]) for m in mats)
+    nb = sum(m[2] for m in mats)
+    for M in (1, 64):
+        Xs = [dev_bf16(synth.workload_activations(4, 10 + i, M, K)) for i, (N, K, _, _) in enumerate(mats)]
+        Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for (N, K, _, _) in mats]
+        with torch.cuda.stream(stream):
+            if M == 1:
+                ws = torch.zeros(max(int(q.lib.q4nx_gemv_workspace(ctypes.byref(mats[0][3][0].c()))), 1 << 16),
+                                 dtype=torch.uint8, device=dev)
+            else:
+                ws = torch.zeros(max(int(q.lib.q4nx_gemm_workspace(ctypes.byref(m[3][0].c()), M)) for m in mats),
+                                 dtype=torch.uint8, device=dev)
+        fns = []
+        for r in range(R):
+            for i, m in enumerate(mats):
+                W = m[3][r]
+                if M == 1:
+                    fns.append(lambda W=W, i=i: q.q4nx_gemv(W, Xs[i][0], out=Ys[i][0], out_dtype="bf16", ws=ws))
+                else:
+                    fns.append(lambda W=W, i=i: q.q4nx_gemm_m64(W, Xs[i], out=Ys[i], out_dtype="bf16", ws=ws))
+        us = timeit(fns, 400) * len(mats)            # per block (one launch per weight)
+        flops = sum(2.0 * M * N * K for (N, K, _, _) in mats)
+        alg = nb + sum(2 * M * K + 2 * M * N for (N, K, _, _) in mats)
+        t_roof = max(alg / (hbm * 1e3), flops / (tc_peak * 1e6))
+        emit({"suite": "block", "workload": "prefill block q4_1 8B width: gate|up 24576x4096, down 4096x12288",
+              "M": M, "launches": len(mats), "us": us, "weight_gbs": nb / us / 1e3, "tflops": flops / us / 1e6,
+              "roofline": {"bound": "hbm" if alg / (hbm * 1e3) >= flops / (tc_peak * 1e6) else "tensor",
+                           "roofline_us": t_roof, "frac": t_roof / us}})
+        del Xs, Ys, ws
+    del mats
+    torch.cuda.empty_cache()
 
 
 def main():
@@ -565,7 +617,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
-    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_small_m,gemm_m64,argmax")
+    ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_small_m,gemm_m64,argmax,block")
     ap.add_argument("--case", default="", help="suite: substring of the workload name")
     args = ap.parse_args()
     if args.warmup < 3:

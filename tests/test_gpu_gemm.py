@@ -73,6 +73,30 @@ def test_gemm_prefill_block_8b_width(q, N, K):
     run(q, synth.Q4_1, N, K, 64, out="bf16", rows=rows)
 
 
+@pytest.mark.parametrize("M", [1, 64])
+def test_merged_gate_up_weight(q, M):
+    """gate and up of the 8B-width block (12288x4096 each) as one 24576x4096
+    weight, their chunk arrays concatenated: rows below 12288 are gate's
+    outputs, the rest up's, each checked against the oracle of its own weight
+    (sampled rows around both ends and the seam)."""
+    Nh, K = 12288, 4096
+    _, wg = synth.make(synth.Q4_1, Nh, K, synth.rng(4, 10, 0))
+    _, wu = synth.make(synth.Q4_1, Nh, K, synth.rng(4, 11, 0))
+    X = synth.activations(synth.rng(4, 12, 0), M, K)
+    W = q.Weight(to_dev_bytes(np.concatenate([wg, wu])), synth.Q4_1, 2 * Nh, K)
+    Xd = to_dev_bf16(X)
+    if M == 1:
+        Y = out_values(q.q4nx_gemv(W, Xd[0].contiguous(), out_dtype="bf16"))[None]
+    else:
+        Y = out_values(q.q4nx_gemm_m64(W, Xd, out_dtype="bf16"))
+    assert Y.shape == (M, 2 * Nh)
+    g = np.random.default_rng(3)
+    for w, base in ((wg, 0), (wu, Nh)):
+        r = np.unique(np.concatenate([np.arange(0, 96), np.arange(Nh - 96, Nh), g.integers(0, Nh, 300)]))
+        Y64, A = oracle.matmul(w, synth.Q4_1, Nh, K, X, rows=r)
+        assert_within(Y[:, base + r], Y64, A, True, f"merged gate|up M={M} half {base // Nh}")
+
+
 def test_gemm_repeat_runs_are_byte_identical(q):
     f, w = synth.make(synth.Q4_1, 4096, 12288, synth.rng(4, 0, 70))
     X = to_dev_bf16(synth.activations(synth.rng(4, 0, 71), 64, 12288))

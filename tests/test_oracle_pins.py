@@ -165,6 +165,18 @@ def test_tile_grid_is_row_major():
 
 
 @pytest.mark.parametrize("kind", KINDS)
+def test_concatenated_chunk_arrays_stack_rows(kind):
+    """The grid is row-major over whole tile rows, so two weights of the same
+    width whose chunk arrays are concatenated form one weight with the first's
+    rows above the second's (how gate and up become one matrix)."""
+    _, wa = synth.make(kind, 64, 512, synth.rng(5, matrix_id=20 + kind))
+    _, wb = synth.make(kind, 96, 512, synth.rng(5, matrix_id=40 + kind))
+    Wab = oracle.weights_f64(np.concatenate([wa, wb]), kind, 160, 512)
+    assert np.array_equal(Wab[:64], oracle.weights_f64(wa, kind, 64, 512))
+    assert np.array_equal(Wab[64:], oracle.weights_f64(wb, kind, 96, 512))
+
+
+@pytest.mark.parametrize("kind", KINDS)
 def test_generator_round_trip(kind):
     g = synth.rng(5, matrix_id=kind)
     f, w = synth.make(kind, 96, 512, g)
