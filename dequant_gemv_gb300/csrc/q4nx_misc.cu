@@ -364,12 +364,18 @@ constexpr int kArgmaxCluster = 8;
 constexpr int kArgmaxThreads = 512;
 
 
-__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
+// BATCH: 16-byte loads a thread has in flight before it uses any.  Few rows
+// (CTAs <= SMs): 12, so that a CTA's eighth of a ~150K-logit row is one round
+// trip; many rows: 4, with the registers of four CTAs per SM.
+template <int BATCH>
+__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads, BATCH > 4 ? 1 : 4)
     argmax_kernel(const float* __restrict__ logits, int64_t V, int32_t* __restrict__ idx) {
   __shared__ uint64_t warp_best[kArgmaxThreads / 32];
   __shared__ uint64_t cta_best;
   cg::cluster_group cluster = cg::this_cluster();
   const unsigned rank = cluster.block_rank();
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // the logits may be the previous grid's output
   const int64_t m = blockIdx.y;
   const float* row = logits + m * V;
   const int64_t per = (V + kArgmaxCluster - 1) / kArgmaxCluster;
@@ -380,29 +386,22 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
   if (vec && b1 > b0) {
     const int64_t n4 = (b1 - b0) / 4;
     const float4* r4 = reinterpret_cast<const float4*>(row + b0);
-    // four loads in flight per thread before any is used: the scan is
-    // latency-bound, not bandwidth-bound, at one row of ~150K logits
-    int64_t i = threadIdx.x;
-    for (; i + 3 * kArgmaxThreads < n4; i += 4 * kArgmaxThreads) {
-      float4 v[4];
+    // every load of a batch is in flight before any is used: the scan is
+    // latency-bound
+    for (int64_t i = threadIdx.x; i < n4; i += BATCH * kArgmaxThreads) {
+      float4 v[BATCH];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldg(r4 + i + u * kArgmaxThreads);
+      for (int u = 0; u < BATCH; ++u)
+        if (i + u * kArgmaxThreads < n4) v[u] = __ldg(r4 + i + u * kArgmaxThreads);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < BATCH; ++u) {
+        if (i + u * kArgmaxThreads >= n4) break;
         const uint32_t k = static_cast<uint32_t>(b0 + 4 * (i + u * kArgmaxThreads));
         best = umax64(best, argmax_key(v[u].x, k));
         best = umax64(best, argmax_key(v[u].y, k + 1));
         best = umax64(best, argmax_key(v[u].z, k + 2));
         best = umax64(best, argmax_key(v[u].w, k + 3));
       }
-    }
-    for (; i < n4; i += kArgmaxThreads) {
-      const float4 v = __ldg(r4 + i);
-      const uint32_t k = static_cast<uint32_t>(b0 + 4 * i);
-      best = umax64(best, argmax_key(v.x, k));
-      best = umax64(best, argmax_key(v.y, k + 1));
-      best = umax64(best, argmax_key(v.z, k + 2));
-      best = umax64(best, argmax_key(v.w, k + 3));
     }
     for (int64_t i = b0 + 4 * n4 + threadIdx.x; i < b1; i += blockDim.x)
       best = umax64(best, argmax_key(__ldg(row + i), static_cast<uint32_t>(i)));
@@ -429,9 +428,23 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
 }
 
 cudaError_t launch_argmax(const float* logits, int M, int64_t V, int32_t* idx, cudaStream_t s) {
-  const dim3 grid(kArgmaxCluster, static_cast<unsigned>(M));
-  argmax_kernel<<<grid, kArgmaxThreads, 0, s>>>(logits, V, idx);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs start while the grid that writes
+  // the logits drains, and wait for it before the first load
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kArgmaxCluster, static_cast<unsigned>(M));
+  cfg.blockDim = dim3(kArgmaxThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (static_cast<int64_t>(M) * kArgmaxCluster <= sms) return cudaLaunchKernelEx(&cfg, argmax_kernel<12>, logits, V, idx);
+  return cudaLaunchKernelEx(&cfg, argmax_kernel<4>, logits, V, idx);
 }
 
 }  // namespace q4nx
