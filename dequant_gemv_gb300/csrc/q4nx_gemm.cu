@@ -26,8 +26,9 @@
 //                bank conflicts) and the scale/zero regions (one 4-D tensor
 //                copy); Q8: the 4 whole chunks (one 4-D tensor copy), whose
 //                column-wise codes the dequant warps read a byte at a time;
-//   warp 1       X producer: the 64 x 256 bf16 slice of X (one 3-D tensor copy
-//                of 4 boxes of 64 x 64) into one of kStages stages;
+//   warp 1       X producer: the tokens' 256-column bf16 slice of X (four 2-D
+//                tensor copies of 64 columns x M tokens rounded up to 8) into
+//                one of kStages stages;
 // The producers, like the MMA warp, run their loops warp-wide and issue from
 // one elected lane: a copy instruction issued from a single-lane branch costs
 // far more issue slots, and these slots are shared with the dequant warps.
@@ -171,9 +172,9 @@ __device__ __forceinline__ void issue_weights_q8(uint32_t dst, const CUtensorMap
       ::"r"(dst), "r"(ks), "r"(tr4), "r"(bar), "n"(4 * kQ8Bytes), "l"(reinterpret_cast<uint64_t>(map))
       : "memory");
 }
-// One k-step of X, on one elected lane: arm `bar` for 32 KB, then copy
-// X[0:64, 256 ks .. +255] as 4 boxes of 64 tokens x 64 k (128-byte swizzle).
-// X of one k-step: four boxes of 64 columns x mrows tokens (M rounded up to 8,
+// One k-step of X, on one elected lane: arm `bar` for the four boxes' bytes,
+// then copy X[0:mrows, 256 ks .. +255] (128-byte swizzle) as four boxes of
+// 64 columns x mrows tokens (M rounded up to 8,
 // so that a box reaches at most 7 token rows past the end of X: boxes mostly
 // outside the tensor are slow to fill), each into its 8 KB slot of the stage.
 // Rows from mrows to 63 of a slot keep whatever they held: they only reach
