@@ -97,3 +97,30 @@ def test_top1_repeat_calls_leave_the_workspace_clean(q):
     torch.cuda.synchronize()
     assert int(ws[4:16].count_nonzero().item()) == 0
     q.q4nx_check(device=DEV)
+
+
+def test_argmax_waits_for_the_gemv_that_writes_its_logits(q):
+    """The argmax starts while the GEMV that writes its logits drains: before
+    every GEMV the buffer holds a planted maximum far above any logit, so an
+    argmax that read it early would return the planted row.  Back to back on
+    one stream, no synchronisation in between."""
+    N, K = 151936, 2560
+    Ws, xs = [], []
+    for s in range(3):
+        _, _, W = _weight(q, synth.Q8_KR, N, K, 30 + s)
+        Ws.append(W)
+        xs.append(to_dev_bf16(synth.activations(synth.rng(5, 1, 30 + s), 1, K)[0]))
+    logits = torch.empty((1, N), dtype=torch.float32, device=DEV)
+    idx = torch.empty(1, dtype=torch.int32, device=DEV)
+    got = []
+    for it in range(12):
+        W, x = Ws[it % 3], xs[it % 3]
+        logits.fill_(0.0)
+        logits[0, (7919 * (it + 1)) % N] = 1e30
+        q.q4nx_gemv(W, x, out=logits[0], out_dtype="f32")
+        q.q4nx_argmax(logits, out=idx)
+        got.append(idx.clone())
+    torch.cuda.synchronize()
+    ref = [int(q.q4nx_gemv_top1(Ws[i], xs[i]).item()) for i in range(3)]
+    for it in range(12):
+        assert int(got[it].item()) == ref[it % 3]
