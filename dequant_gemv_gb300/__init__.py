@@ -402,11 +402,18 @@ def q4nx_argmax(logits: torch.Tensor, out: torch.Tensor | None = None) -> torch.
 
 def q4nx_check(ws: torch.Tensor | None = None, device=None) -> None:
     """Raise if a bounded in-kernel wait of an earlier call on this workspace (default:
-    this stream's GEMV and GEMM workspaces) gave up."""
+    this stream's GEMV and GEMM workspaces) gave up.  A workspace that reports
+    such an error must be zero-filled before its next use: the default ones
+    are zero-filled here before raising; a caller's own `ws` is left to the
+    caller."""
     if ws is not None:
         _check(lib.q4nx_check(ws.data_ptr(), _stream(ws.device)), "q4nx_check")
         return
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     for family in WS_FAMILIES:
         w = workspace(device, 16, family)
-        _check(lib.q4nx_check(w.data_ptr(), _stream(w.device)), "q4nx_check")
+        st = lib.q4nx_check(w.data_ptr(), _stream(w.device))
+        if st != 0:
+            with torch.cuda.device(w.device):
+                w.zero_()
+        _check(st, "q4nx_check")

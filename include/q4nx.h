@@ -174,8 +174,9 @@ uint64_t q4nx_gemv_batch_workspace(const q4nx_gemv_item* items, int count);
  * bf16-rounded weights, each within 2^-9 of itself, so an output may differ
  * from the exact sum by that much of sum_k |w x| beyond the fp32 rounding.
  * workspace_dev: at least q4nx_gemm_workspace(w, M) bytes (the same for every
- * M), zero-filled before first use; it holds the error word, and calls may
- * leave partial sums in it, so it is not shared with the GEMV entry points. */
+ * M), zero-filled before first use and again after Q4NX_E_DEVICE_TIMEOUT; it
+ * holds the error word, and calls may leave partial sums in it, so it is not
+ * shared with the GEMV entry points. */
 int q4nx_gemm_m64(const q4nx_weight* w, const void* X_dev, int M, void* Y_dev, int out_dtype,
                   void* workspace_dev, uint64_t workspace_bytes, void* stream);
 uint64_t q4nx_gemm_workspace(const q4nx_weight* w, int M);
@@ -234,7 +235,9 @@ uint64_t q4nx_noalloc_scratch_bytes(void);
 
 /* Read and clear the error word of a workspace (synchronises `stream`).
  * Returns Q4NX_OK, or Q4NX_E_DEVICE_TIMEOUT if a bounded in-kernel wait of a
- * call that used this workspace gave up (its outputs are then invalid). */
+ * call that used this workspace gave up (its outputs are then invalid, and
+ * the workspace must be zero-filled before it is used again: the calls that
+ * gave up may have left counters and posted sums in it). */
 int q4nx_check(void* workspace_dev, void* stream);
 
 #ifdef __cplusplus

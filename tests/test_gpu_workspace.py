@@ -85,3 +85,59 @@ def test_gemv_after_gemm_on_one_stream(q):
     got = y1.cpu().numpy().astype(np.float64)[rows]
     assert np.all(np.abs(got - Y64) <= 1e-3 * A)
     q.q4nx_check()
+
+
+def _planted_gemm(q):
+    """A GEMM whose first tile is split between CTAs (1024x4096, M = 64: 32
+    CTAs of 4 k-steps each, tile 0 finished by CTA 0 once its 3 contributors
+    have counted themselves in)."""
+    kind, N, K = synth.Q4_1, 1024, 4096
+    f, w = synth.make(kind, N, K, synth.rng(21, 40, 0))
+    X = synth.activations(synth.rng(21, 41, 0), 64, K)
+    W = q.Weight(torch.from_numpy(w).to(DEV), kind, N, K)
+    Xd = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).to(DEV).view(torch.bfloat16)
+    need = int(q.lib.q4nx_gemm_workspace(ctypes.byref(W.c()), 64))
+    return w, X, W, Xd, need
+
+
+def _plant(ws):
+    """Tile 0's posting counter (the u32 after the 16-byte error block) far
+    above any count its contributors can reach: the finisher's wait cannot
+    succeed."""
+    ws.zero_()
+    ws[16:20] = torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8, device=ws.device)
+
+
+def test_gemm_bounded_wait_reports_timeout_and_recovers(q):
+    """A wait that cannot succeed gives up after its bounded time: the launch
+    completes, q4nx_check reports Q4NX_E_DEVICE_TIMEOUT, and the context and
+    the library stay usable; with the workspace zero-filled again the same
+    call is correct."""
+    kind, N, K = synth.Q4_1, 1024, 4096
+    w, X, W, Xd, need = _planted_gemm(q)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    _plant(ws)
+    q.q4nx_gemm_m64(W, Xd, out_dtype="f32", ws=ws)
+    with pytest.raises(q.Q4NXError) as e:
+        q.q4nx_check(ws)
+    assert e.value.status == 10                                        # Q4NX_E_DEVICE_TIMEOUT
+    ws.zero_()
+    Y = q.q4nx_gemm_m64(W, Xd, out_dtype="f32", ws=ws).cpu().numpy().astype(np.float64)
+    q.q4nx_check(ws)
+    Y64, A = oracle.matmul(w, kind, N, K, X)
+    assert np.all(np.abs(Y - Y64) <= (1e-3 + 2.0 ** -9) * A)
+
+
+def test_default_workspace_is_zeroed_after_a_reported_timeout(q):
+    """The binding's own GEMM workspace: q4nx_check raises and zero-fills it,
+    so the next call through the default workspace is correct."""
+    kind, N, K = synth.Q4_1, 1024, 4096
+    w, X, W, Xd, need = _planted_gemm(q)
+    _plant(q.workspace(torch.device(DEV), need, "gemm"))
+    q.q4nx_gemm_m64(W, Xd, out_dtype="f32")
+    with pytest.raises(q.Q4NXError):
+        q.q4nx_check()
+    Y = q.q4nx_gemm_m64(W, Xd, out_dtype="f32").cpu().numpy().astype(np.float64)
+    q.q4nx_check()
+    Y64, A = oracle.matmul(w, kind, N, K, X)
+    assert np.all(np.abs(Y - Y64) <= (1e-3 + 2.0 ** -9) * A)
