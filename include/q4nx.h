@@ -103,7 +103,11 @@ int q4nx_decode(const q4nx_weight* w, void* out_dev, uint64_t out_bytes, void* s
  * again (after Q4NX_E_DEVICE_TIMEOUT it must be zero-filled anew).  It holds
  * an error word and the partial sums of tile rows split between CTAs, each
  * posted with a ready flag (16 B + 256 KiB for any weight).
- * Results are deterministic: partials are added in a fixed order. */
+ * Results are deterministic: partials are added in a fixed order.  A tile row
+ * split between CTAs is finished by the CTA that holds its first chunk once
+ * the later CTAs (at most one per SM) have posted; they get SMs as soon as
+ * any frees, and a wait that still runs out reports Q4NX_E_DEVICE_TIMEOUT
+ * through q4nx_check. */
 int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype,
               void* workspace_dev, uint64_t workspace_bytes, void* stream);
 uint64_t q4nx_gemv_workspace(const q4nx_weight* w);
