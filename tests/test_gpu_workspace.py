@@ -141,3 +141,28 @@ def test_default_workspace_is_zeroed_after_a_reported_timeout(q):
     q.q4nx_check()
     Y64, A = oracle.matmul(w, kind, N, K, X)
     assert np.all(np.abs(Y - Y64) <= (1e-3 + 2.0 ** -9) * A)
+
+
+def test_gemv_on_two_streams_at_once(q):
+    """Two streams, each with its own workspace (the binding keys them by
+    stream), running GEMVs of different weights concurrently: every result
+    equals the same call made alone."""
+    kind = synth.Q4_1
+    a = _weight(q, kind, 12288, 4096, 50)
+    b = _weight(q, kind, 4096, 12288, 51)
+    ref_a = q.q4nx_gemv(a[2], a[3], out_dtype="f32").clone()
+    ref_b = q.q4nx_gemv(b[2], b[3], out_dtype="f32").clone()
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    outs_a, outs_b = [], []
+    for _ in range(8):
+        with torch.cuda.stream(s1):
+            outs_a.append(q.q4nx_gemv(a[2], a[3], out_dtype="f32"))
+        with torch.cuda.stream(s2):
+            outs_b.append(q.q4nx_gemv(b[2], b[3], out_dtype="f32"))
+    torch.cuda.synchronize()
+    for ya, yb in zip(outs_a, outs_b):
+        assert torch.equal(ya, ref_a) and torch.equal(yb, ref_b)
+    for s in (s1, s2):
+        with torch.cuda.stream(s):
+            q.q4nx_check()
