@@ -56,8 +56,10 @@
 // while the others (which hold the tile's later k-steps at the start of their
 // ranges) post their fp32 partials early; the finisher gathers them into its
 // epilogue warps' registers while its own main loop still runs, then adds
-// them to its accumulator.  The sum order is fixed (the other CTAs' partials in CTA order,
-// then the finisher's own), so results are deterministic.  Every wait is
+// them to its accumulator.  The sum order depends only on the shape (the next
+// CTA's partial, those beyond the shared-memory gather slots, the gathered
+// ones, each group in CTA order, then the finisher's own), so results are
+// deterministic.  Every wait is
 // bounded; if one gives up, the CTA records the error in the workspace and
 // winds down.
 //
@@ -611,8 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = lo <= u_lo && u_hi <= hi;   // the whole tile is computed here
       const bool contrib = u_lo < lo;                // another CTA holds the tile's first k-step
       const bool finisher = !whole && !contrib;
-      // finisher: the later CTAs' partials of this thread's row, summed in CTA
-      // order, gathered before the accumulator is ready (token quad k in fx[k])
+      // finisher: the later CTAs' partials of this thread's row, summed in an
+      // order fixed by the shape, gathered before the accumulator is ready
+      // (token quad k in fx[k])
       float4 fx[kTileN / 4];
       const bool last = t == ntiles - 1;
       if (finisher) {

@@ -60,6 +60,16 @@ def test_gemm_single_k_step(q, kind, N, M):
     run(q, kind, N, 256, M, wid=5 if kind != synth.Q4_1 else 4)
 
 
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q8_KR, synth.Q8_BLK])
+@pytest.mark.parametrize("N,K", [(128, 12288), (96, 16384), (256, 12288)])
+@pytest.mark.parametrize("M", [64, 17])
+def test_gemm_tile_split_many_ways(q, kind, N, K, M):
+    """Narrow, deep weights: a 128-row tile's k-steps spread over 8-16 CTAs,
+    so its finisher takes the later partials through all 5 shared-memory
+    gather slots and reads the rest directly."""
+    run(q, kind, N, K, M, wid=5 if kind != synth.Q4_1 else 4)
+
+
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_gemm_q4_1_output_dtypes(q, out):
     run(q, synth.Q4_1, 512, 1536, 64, out=out)
