@@ -67,6 +67,19 @@ def test_tokens_match_oracle(q, kind, N, K, M, out):
     assert torch.equal(Y.view(bits), again.view(bits)), "a repeated call gave different bits"
 
 
+@pytest.mark.parametrize("M", [2, 4])
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K])
+def test_tokens_row_split_over_many_ctas(q, kind, M):
+    """64 x 65536: each tile row's 256 chunks spread over 64 CTAs, whose
+    per-token row sums the owner of the row's first chunk adds up."""
+    N, K = 64, 65536
+    w, X, W, Xd = _case(q, kind, N, K, M, 70 + M)
+    got = out_values(q.q4nx_gemm_m64(W, Xd, out_dtype="f32"))
+    Y64, A = oracle.matmul(w, kind, N, K, X)
+    assert_within(got, Y64, A, False, f"tokens kind {kind} {N}x{K} M={M}",
+                  bf16_weights=tensor_path(kind, M) and K < 2560)
+
+
 def test_q4k_tokens_then_unsupported_beyond(q):
     w, X, W, Xd = _case(q, synth.Q4_K, 2560, 9728, 5, 90)
     rows = np.arange(0, 2560, 5)
