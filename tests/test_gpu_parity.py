@@ -305,7 +305,8 @@ def test_repacked_weights_run_on_q4_1_gemv(q):
 
 # ------------------------------------------------------------------ argmax --
 
-@pytest.mark.parametrize("M,V", [(1, 1), (1, 7), (3, 1000), (1, 151936), (64, 151936), (5, 151937), (2, 33)])
+@pytest.mark.parametrize("M,V", [(1, 1), (1, 7), (3, 1000), (1, 151936), (64, 151936), (5, 151937), (2, 33),
+                                 (19, 151936), (20, 151936), (1, 1 << 20), (2, 1000003)])
 def test_argmax_bit_exact(q, M, V):
     g = np.random.default_rng(M * 7 + V)
     L = g.normal(size=(M, V)).astype(np.float32)
