@@ -30,6 +30,9 @@ import torch
 
 Q4NX_Q4_1, Q4NX_Q4_K, Q4NX_Q8_KR, Q4NX_Q8_BLK = 1, 2, 3, 4
 Q4NX_OUT_BF16, Q4NX_OUT_F32 = 0, 1
+# statuses of include/q4nx.h
+(Q4NX_OK, Q4NX_E_NULL, Q4NX_E_KIND, Q4NX_E_SHAPE, Q4NX_E_SHORT, Q4NX_E_ALIGN, Q4NX_E_M, Q4NX_E_WORKSPACE,
+ Q4NX_E_UNSUPPORTED, Q4NX_E_CUDA, Q4NX_E_DEVICE_TIMEOUT, Q4NX_E_DTYPE) = range(12)
 KINDS = {"q4_1": Q4NX_Q4_1, "q4_k": Q4NX_Q4_K, "q8_kr": Q4NX_Q8_KR, "q8_blk": Q4NX_Q8_BLK}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -413,7 +416,7 @@ def q4nx_check(ws: torch.Tensor | None = None, device=None) -> None:
     for family in WS_FAMILIES:
         w = workspace(device, 16, family)
         st = lib.q4nx_check(w.data_ptr(), _stream(w.device))
-        if st != 0:
+        if st != Q4NX_OK:
             with torch.cuda.device(w.device):
                 w.zero_()
         _check(st, "q4nx_check")

@@ -30,6 +30,17 @@ def _declared():
     return sorted(set(re.findall(r"\b(q4nx_[a-z0-9_]+)\s*\(", src)))
 
 
+def test_binding_constants_match_the_header(q):
+    """The binding's status, kind and output-type numbers are the header's."""
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "q4nx.h")).read(), flags=re.S)
+    vals = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(Q4NX_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    for name in ("Q4NX_OK", "Q4NX_E_NULL", "Q4NX_E_KIND", "Q4NX_E_SHAPE", "Q4NX_E_SHORT", "Q4NX_E_ALIGN",
+                 "Q4NX_E_M", "Q4NX_E_WORKSPACE", "Q4NX_E_UNSUPPORTED", "Q4NX_E_CUDA", "Q4NX_E_DEVICE_TIMEOUT",
+                 "Q4NX_E_DTYPE", "Q4NX_Q4_1", "Q4NX_Q4_K", "Q4NX_Q8_KR", "Q4NX_Q8_BLK", "Q4NX_OUT_BF16",
+                 "Q4NX_OUT_F32"):
+        assert getattr(q, name) == vals[name], name
+
+
 def test_exports_every_declared_symbol(q):
     names = _declared()
     assert "q4nx_gemv" in names and "q4nx_gemm_m64" in names and len(names) >= 11

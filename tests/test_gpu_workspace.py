@@ -120,7 +120,7 @@ def test_gemm_bounded_wait_reports_timeout_and_recovers(q):
     q.q4nx_gemm_m64(W, Xd, out_dtype="f32", ws=ws)
     with pytest.raises(q.Q4NXError) as e:
         q.q4nx_check(ws)
-    assert e.value.status == 10                                        # Q4NX_E_DEVICE_TIMEOUT
+    assert e.value.status == q.Q4NX_E_DEVICE_TIMEOUT
     ws.zero_()
     Y = q.q4nx_gemm_m64(W, Xd, out_dtype="f32", ws=ws).cpu().numpy().astype(np.float64)
     q.q4nx_check(ws)
