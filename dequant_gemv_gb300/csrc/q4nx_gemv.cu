@@ -8,7 +8,8 @@
 // kind (a single GEMV is a batch of one), or one weight against MT tokens.
 //
 // Design (HBM-bound: 0.625 B/weight for q4_1):
-//  * Persistent grid, one CTA per SM.  The chunks of all items form one index
+//  * Persistent grid, one CTA per SM (two for 4-bit launches of 128 chunks or
+//    more per SM, each within half an SM).  The chunks of all items form one index
 //    space (item after item, each row-major over its tile grid); CTA b owns an
 //    even contiguous share, each warp a contiguous part of it.  A range is a
 //    run of (item, tile row) segments.
@@ -627,6 +628,9 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
 
 // ----------------------------------------------------------------- host ----
 
+// Chunks per SM from which a 4-bit single-token launch runs two CTAs per SM.
+constexpr int kTwoCtaChunksPerSm = 128;
+
 static int gemv_max_warps(int kind, int MT) {
   const bool q4 = kind == kQ4_1 || kind == kQ4_K;
   return MT == 1 ? 8 : (MT == 2 && q4) ? 12 : 8;
@@ -664,9 +668,20 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
   if (!warps) return false;
   // One CTA per SM; small problems use fewer CTAs of at least ~4 chunks each so
   // that split tile rows are combined inside a CTA rather than across CTAs.
+  // Large 4-bit launches (at least kTwoCtaChunksPerSm chunks per SM, ~100 MB)
+  // take both half-SM slots of every SM themselves: twice the copies in flight
+  // while they stream.  Measured on GB300, back to back: the 196-matrix decode
+  // step and a 151936x2560 weight 2.3-2.5 % faster.  The price is paid by the
+  // launch after it, which can start its first copies only as this one's CTAs
+  // exit: a 4096x12288 GEMV behind a 24576x4096 one (81 chunks per SM) lost
+  // 2.3 us that way, more than the 0.5 us the larger launch gained, so
+  // launches of that size keep one CTA per SM and leave the second slot to the
+  // next launch (below ~60 chunks per SM two CTAs are slower even back to back:
+  // 12288x4096 8.4 -> 9.0 us).
+  const bool two_per_sm = CB <= kQ41Bytes && MT == 1 && T >= static_cast<int64_t>(kTwoCtaChunksPerSm) * info.sms;
   int64_t grid = T / 4;
   if (grid < 1) grid = 1;
-  if (grid > info.sms) grid = info.sms;
+  if (grid > (two_per_sm ? 2 : 1) * static_cast<int64_t>(info.sms)) grid = (two_per_sm ? 2 : 1) * static_cast<int64_t>(info.sms);
   if (grid > kMaxCtas) grid = kMaxCtas;
   const int64_t per_cta = T / grid;                // every warp gets at least one chunk
   if (per_cta < warps) warps = static_cast<int>(per_cta);

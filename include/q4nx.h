@@ -105,7 +105,7 @@ int q4nx_decode(const q4nx_weight* w, void* out_dev, uint64_t out_bytes, void* s
  * posted with a ready flag (16 B + 256 KiB for any weight).
  * Results are deterministic: partials are added in a fixed order.  A tile row
  * split between CTAs is finished by the CTA that holds its first chunk once
- * the later CTAs (at most one per SM) have posted; they get SMs as soon as
+ * the later CTAs (at most two per SM) have posted; they get SMs as soon as
  * any frees, and a wait that still runs out reports Q4NX_E_DEVICE_TIMEOUT
  * through q4nx_check. */
 int q4nx_gemv(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype,

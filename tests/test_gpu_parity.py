@@ -171,6 +171,29 @@ def test_gemv_workload_sizes(q, kind, N, K, wid, out):
     assert_within(y if rows is None else y[rows], Y64, A, out == "bf16", f"kind {kind} {N}x{K}")
 
 
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K])
+def test_gemv_two_ctas_per_sm_threshold(q, kind):
+    """A 4-bit weight of at least 128 chunks per SM runs two CTAs per SM, a smaller
+    one a single CTA per SM: shapes on both sides of that point, one of them with
+    tile rows of 152 chunks spread over several CTAs, match the oracle on sampled
+    rows, and a repeated call gives the same bytes."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = [(4 * sms, 32), (4 * sms - 1, 32), (-(-128 * sms // 152), 152)]   # (tile rows, tile columns)
+    for i, (TR, TC) in enumerate(shapes):
+        N, K = 32 * TR, 256 * TC
+        f, w = synth.make(kind, N, K, synth.rng(12, kind, i))
+        W = q.Weight(to_dev_bytes(w), kind, N, K)
+        x = synth.activations(synth.rng(12, 1, i), 1, K)[0]
+        xd = to_dev_bf16(x)
+        yd = q.q4nx_gemv(W, xd, out_dtype="f32").clone()
+        again = q.q4nx_gemv(W, xd, out_dtype="f32")
+        assert torch.equal(yd.view(torch.int32), again.view(torch.int32)), f"{N}x{K} not repeatable"
+        rows = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N), np.arange(0, N, 7)]))
+        Y64, A = oracle.matmul(w, kind, N, K, x, rows=rows)
+        assert_within(out_values(yd)[rows], Y64, A, False, f"kind {kind} {N}x{K}")
+    q.q4nx_check(device=DEV)
+
+
 def test_gemv_wide_k(q):
     """Any number of columns (x is streamed with each chunk, not staged whole)."""
     for kind in (synth.Q4_1, synth.Q8_BLK):
