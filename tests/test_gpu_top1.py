@@ -55,7 +55,9 @@ def test_top1_lm_head_matches_argmax_of_the_logits_and_the_oracle(q, kind):
 
 
 @pytest.mark.parametrize("kind,N,K", [(synth.Q4_1, 12288, 4096), (synth.Q4_K, 9728, 2560), (synth.Q4_1, 1024, 1024),
-                                      (synth.Q8_KR, 4096, 2560), (synth.Q4_1, 64, 65536), (synth.Q8_BLK, 64, 65536)])
+                                      (synth.Q8_KR, 4096, 2560), (synth.Q4_1, 64, 65536), (synth.Q8_BLK, 64, 65536),
+                                      # 4-bit weights large enough for two CTAs per SM
+                                      (synth.Q4_1, 151936, 2560), (synth.Q4_K, 4864, 38912)])
 def test_top1_other_kinds_and_sizes(q, kind, N, K):
     f, w, W = _weight(q, kind, N, K, 12, wid=4)
     x = to_dev_bf16(synth.activations(synth.rng(4, 1, 12), 1, K)[0])
