@@ -78,6 +78,13 @@ struct GemvArgsT {
 
 // This CTA's largest top-1 key so far (top-1 mode).
 __shared__ unsigned long long s_top1_key;
+// Where each warp's range starts, relative to the CTA's, and the last CTA that
+// holds part of the tile row at the end of this CTA's range.  Both are worked
+// out before the kernel waits on the previous grid: the row sums at the end of
+// a launch then need no 64-bit division, which cost 0.3-0.7 us a launch on
+// that critical path.
+__shared__ uint32_t s_wlo[32];
+__shared__ long long s_clast;
 
 // Lane-wise transpose-reduce of 8 values over the 8 lanes selected by masks
 // (m2, m1, m0): afterwards the lane whose mask bits read (b2 b1 b0) holds the
@@ -147,7 +154,7 @@ __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t
       if (tok < m) st_relaxed_u64(&a.posted[(b * MT + tok) * 32 + lane], kPosted | __float_as_uint(val[tok]));
     return;
   }
-  const int64_t c_last = cta_of(r1 - 1, a.T, a.grid);
+  const int64_t c_last = s_clast;                     // cta_of(r1 - 1), worked out at the start
   float sum[MT];
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok) sum[tok] = val[tok];
@@ -428,11 +435,6 @@ struct Pos {
 
 // ----------------------------------------------------- segment results ----
 
-// Warp of a CTA owning chunks [Lc, Hc) split over nw warps that holds chunk c.
-__device__ __forceinline__ int warp_of(int64_t c, int64_t Lc, int64_t Hc, int nw) {
-  return static_cast<int>(((c - Lc + 1) * nw - 1) / (Hc - Lc));
-}
-
 // End of a segment (item it, tile row tr) of warp w (range [lo, hi)); each
 // lane holds, per token, the sum of the row `row`.  A row held by this warp
 // alone is stored at once.  A row shared with other warps of the CTA is parked
@@ -456,9 +458,12 @@ __device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_
   const int k = (r0 <= lo) ? 0 : 1;                 // the warp's first segment iff the row holds lo
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok) slots[((w * 2 + k) * MT + tok) * 32 + row] = val[tok];
-  const int wa = warp_of(r0 > Lc ? r0 : Lc, Lc, Hc, nw);
-  const int wb = warp_of((r1 < Hc ? r1 : Hc) - 1, Lc, Hc, nw);
-  const int64_t lo_a = Lc + ((Hc - Lc) * wa) / nw;
+  // first and last warp holding part of the row: the warps whose ranges start
+  // at or before the row's first and last chunk in this CTA, counted by ballot
+  const uint32_t wlo = lane < nw ? s_wlo[lane] : 0xFFFFFFFFu;
+  const int wa = __popc(__ballot_sync(0xffffffffu, wlo <= static_cast<uint32_t>((r0 > Lc ? r0 : Lc) - Lc))) - 1;
+  const int wb = __popc(__ballot_sync(0xffffffffu, wlo <= static_cast<uint32_t>((r1 < Hc ? r1 : Hc) - 1 - Lc))) - 1;
+  const int64_t lo_a = Lc + __shfl_sync(0xffffffffu, wlo, wa);
   const int ka = (r0 <= lo_a) ? 0 : 1;             // the row's slot in its first warp
   __threadfence_block();
   __syncwarp();
@@ -540,6 +545,13 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       issue_chunk<KIND, MT>(a, p, m, ring + s * SB, &bars[s]);
       p.next(a);
     }
+  }
+  if (warp == 0 && lane < nwarps) s_wlo[lane] = static_cast<uint32_t>(((Hc - Lc) * lane) / nwarps);
+  if (threadIdx.x == blockDim.x - 1) {
+    Pos e{};
+    e.seek(a, Hc - 1);
+    const int64_t r1 = a.items[e.it].cbase + (static_cast<int64_t>(e.tr) + 1) * a.items[e.it].TC;
+    s_clast = r1 > Hc ? cta_of(r1 - 1, a.T, a.grid) : b;
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
   if (lane == 0) {
