@@ -603,6 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpEpi0) {
     // ----------------------------------------------------------- epilogue
+    // Only a CTA's last tile can be one it finishes (its first k-step here,
+    // later ones in other CTAs); the last CTA holding part of it is worked out
+    // now, before the wait: a 64-bit division at the end of the launch sits on
+    // its critical path.
+    const int64_t c_last_tile = ((last_tile + 1) * KS * a.grid - 1) / a.units;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // Y and the workspace may be the previous grid's
     const int e = warp & 3;                         // TMEM lane quarter of this warp
     const int row = 32 * e + lane;                  // row within the 128-row tile
@@ -620,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool last = t == ntiles - 1;
       if (finisher) {
         // each posting CTA counts once per epilogue warp
-        const int64_t c_last = (u_hi * a.grid - 1) / a.units;
+        const int64_t c_last = c_last_tile;          // (u_hi * grid - 1) / units: this is the last tile
         if (!wait_posted(sh, &a.counters[tile], static_cast<uint32_t>(4 * (c_last - blockIdx.x)), a.err, lane))
           break;
         const float4* p = reinterpret_cast<const float4*>(a.partials + (blockIdx.x + 1) * (kTileN * kTileM)) + row;
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // should be visible as soon as possible.)
         const uint32_t stg = smem_u32(smem + kXOff);
         if (finisher) {
-          const int64_t later = (u_hi * a.grid - 1) / a.units - blockIdx.x - 1;   // partials past the first
+          const int64_t later = c_last_tile - blockIdx.x - 1;   // partials past the first
           const int nsm = static_cast<int>(later < kGatherSlots ? later : kGatherSlots);
           if (nsm > 0) {
             if (warp == kWarpEpi0 && lane == 0) {
