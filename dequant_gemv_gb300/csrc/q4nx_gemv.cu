@@ -158,11 +158,16 @@ __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t
   float sum[MT];
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok) sum[tok] = val[tok];
-  for (int64_t c = b + 1; c <= c_last; ++c) {
+  // With several contributors (a tile row of 38-48 chunks spreads over 2-3
+  // CTAs) their words are loaded kBatch CTAs at a time, so that the L2 round
+  // trips overlap; they are added in CTA order all the same.  One contributor
+  // (the common case) takes the plain loop.
+  constexpr int kBatch = 4;
+  if (c_last == b + 1) {
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok) {
       if (tok >= m) break;
-      uint64_t* p = &a.posted[(c * MT + tok) * 32 + lane];
+      uint64_t* p = &a.posted[((b + 1) * MT + tok) * 32 + lane];
       uint64_t w = ld_relaxed_u64(p);
       if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
         const uint64_t t0 = globaltimer_ns();
@@ -177,6 +182,38 @@ __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t
       }
       sum[tok] += __uint_as_float(static_cast<uint32_t>(w));
       *p = 0ull;                                      // leave the workspace zero-filled
+    }
+  }
+  for (int64_t c0 = b + 1; c_last > b + 1 && c0 <= c_last; c0 += kBatch) {
+    uint64_t wb[kBatch][MT];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+      for (int tok = 0; tok < MT; ++tok)
+        wb[i][tok] = (c0 + i <= c_last && tok < m) ? ld_relaxed_u64(&a.posted[((c0 + i) * MT + tok) * 32 + lane]) : 0ull;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int64_t c = c0 + i;
+      if (c > c_last) break;
+#pragma unroll
+      for (int tok = 0; tok < MT; ++tok) {
+        if (tok >= m) break;
+        uint64_t* p = &a.posted[(c * MT + tok) * 32 + lane];
+        uint64_t w = wb[i][tok];
+        if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
+          const uint64_t t0 = globaltimer_ns();
+          while ((w & kPosted) == 0) {
+            w = ld_relaxed_u64(p);
+            if ((w & kPosted) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+          }
+          if (!__all_sync(0xffffffffu, (w & kPosted) != 0)) {
+            if (lane == 0) atomicOr(a.err, 1u);
+            return;
+          }
+        }
+        sum[tok] += __uint_as_float(static_cast<uint32_t>(w));
+        *p = 0ull;                                    // leave the workspace zero-filled
+      }
     }
   }
 #pragma unroll
