@@ -590,6 +590,12 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     const int64_t r1 = a.items[e.it].cbase + (static_cast<int64_t>(e.tr) + 1) * a.items[e.it].TC;
     s_clast = r1 > Hc ? cta_of(r1 - 1, a.T, a.grid) : b;
   }
+  if (lane < 2) cnt[warp * 2 + lane] = 0u;
+  if (threadIdx.x == 0) s_top1_key = 0ull;
+  __syncwarp();
+  // the row counters are zero and the tables written before any warp can
+  // count; done before the wait, so that no CTA-wide barrier follows it
+  __syncthreads();
   asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
   if (lane == 0) {
     for (int s = 0; s < stages && s < n; ++s) {
@@ -597,10 +603,6 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       pre.next(a);
     }
   }
-  if (lane < 2) cnt[warp * 2 + lane] = 0u;
-  if (threadIdx.x == 0) s_top1_key = 0ull;
-  __syncwarp();
-  __syncthreads();                          // the row counters are zero before any warp can count
 
   float yacc[MT][8];
 #pragma unroll
