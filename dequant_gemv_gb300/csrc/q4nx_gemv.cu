@@ -83,7 +83,8 @@ __shared__ unsigned long long s_top1_key;
 // out before the kernel waits on the previous grid: the row sums at the end of
 // a launch then need no 64-bit division, which cost 0.3-0.7 us a launch on
 // that critical path.
-__shared__ uint32_t s_wlo[32];
+constexpr int kMaxGemvWarps = 16;          // warps per CTA the plan may choose (12 at most today)
+__shared__ uint32_t s_wlo[kMaxGemvWarps];
 __shared__ long long s_clast;
 
 // Lane-wise transpose-reduce of 8 values over the 8 lanes selected by masks
@@ -704,13 +705,16 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
   // dependent launch) starts its weight copies on the same SMs while this one
   // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
   // chunks are larger and gain more from a deeper ring than from that overlap.
-  // (less 256 bytes for the kernel's static shared memory, 128 bytes today)
+  // (less 512 bytes for the kernel's static shared memory, 256 bytes today:
+  // two CTAs of a two-per-SM launch must both fit, or its cross-CTA row sums
+  // would wait on a CTA that has no SM)
   // Several tokens need more registers than two CTAs per SM leave, so those
   // launches take the whole of the shared memory.
   const uint64_t cap =
-      static_cast<uint64_t>(CB <= kQ41Bytes && MT == 1 ? info.smem_two_per_sm : info.max_smem_optin) - 256;
+      static_cast<uint64_t>(CB <= kQ41Bytes && MT == 1 ? info.smem_two_per_sm : info.max_smem_optin) - 512;
   const int max_warps = gemv_max_warps(kind, MT);
   static const int kWarpChoices[] = {12, 8, 6, 4, 2, 1};
+  static_assert(12 <= kMaxGemvWarps, "warp table");
   int warps = 0, stages = 0;
   for (int w : kWarpChoices) {
     if (w > max_warps) continue;
