@@ -20,9 +20,11 @@
 //    before the kernel waits on the previous grid (weights never change
 //    between launches); x only after.
 //  * 4-bit kinds: the lanes first read their share of the stage into
-//    registers and the stage is refilled at once; then x becomes 16-bit fixed
-//    point per 32-column group (two byte planes) and the code dot products are
-//    exact dp4a integer sums; scale and zero are applied per (row, group).
+//    registers and the stage is refilled at once; then x becomes 24-bit fixed
+//    point per 32-column group (three signed digit planes) and the code dot
+//    products are exact dp4a integer sums; scale and zero are applied per
+//    (row, group, plane), each plane's partial rounded once.  A chunk whose x
+//    groups that fixed point cannot hold exactly takes a binary32 path.
 //  * Q8 kinds: codes become exact floats through the 2^23 magic number and
 //    packed fp32 FMAs; d scales each lane's (row, group) partial.
 //  * Row sums are finished with a warp transpose-reduce.  A tile row split
@@ -37,7 +39,7 @@
 namespace q4nx {
 
 constexpr int kXSliceBytes = 512;            // bf16 x of one tile column, per token
-constexpr int kScratchBytes = 512;           // per warp and token: x byte planes of one chunk
+constexpr int kScratchBytes = 768;           // per warp and token: x digit planes (or the raw x slice) of one chunk
 constexpr int kSlotBytes = 2 * 32 * 4;       // per warp and token: sums of its first and last tile row
 constexpr int kCntBytes = 8;                 // per warp: arrival counters of its first and last tile row
 constexpr int kMaxBatch = kMaxGemvItems;
@@ -224,17 +226,29 @@ __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t
 
 // ------------------------------------------------------- chunk bodies ----
 
-// q4 kinds.  Per chunk, the warp first turns the 256-wide bf16 x slice into
-// 16-bit fixed point per 32-column group: q_k = round(x_k 2^(141 - E_g)),
-// E_g the biased exponent of max |x| over the group, so |q_k| <= 255 * 128
-// (a bf16 has 8 significant bits) and the rounding error is at most 2^-16 of
-// the group's largest |x|.  q = 256 P1 + P0 is kept as two byte planes (P0
-// unsigned, P1 signed), packed four columns to a word in the order dp4a meets
-// the codes: low nibbles (even k) and high nibbles (odd k) of a code word.
-// Then for each (row, group) the code dot product is exact integer work:
-//   S0 = sum c P0, S1 = sum c P1 (dp4a, 4 codes per instruction),
-//   sum_k c_k x_k = (256 S1 + S0) 2^(E_g - 141)
-// and y_r += s_rg (sum_k c_k x_k) + z_rg X_g with X_g = sum_k x_k in fp32.
+// q4 kinds.  The 32 x 256 codes are multiplied with x in exact integer
+// arithmetic.  Per chunk and token, the warp writes each 32-column group of
+// the bf16 x slice as 24-bit fixed point: v_k = x_k 2^(148 - E), E the biased
+// exponent of the group's largest |x|, so |v_k| < 2^22.  This is exact when
+// every nonzero x_k of the group lies within 2^14 of the largest (its lowest
+// significant bit is then a multiple of the step 2^(E-148)) and 22 <= E <= 254.
+// v_k + 0x808080 split into bytes gives three signed digits, v_k =
+// d0 + 256 d1 + 65536 d2 with d_p in [-128, 127], kept as three byte planes
+// packed four columns to a word in the order dp4a meets the codes: low
+// nibbles (even k) and high nibbles (odd k) of a code word.  For each
+// (row r, group g) and plane p the code dot product is an exact integer,
+//   S_p = sum_k c_k d_p[k]  (dp4a, 4 codes per instruction, |S_p| <= 61440),
+// and with X_p = sum_k d_p[k] and the plane weight q_p = 2^(E - 148 + 8p):
+//   sum_k (c_k s + z) x_k = sum_p (s S_p q_p + z X_p q_p).
+// S_p q_p and z X_p q_p are exact in binary32 (z has 8 significant bits for
+// q4_1, |X_p| <= 4096), so each plane's partial s S_p q_p + z X_p q_p is
+// rounded once (one fma), relative to its own exact value: there is no
+// cancellation between the scale and the zero terms.  Q4_K's zero M*mn has up
+// to 14 significant bits, so its z X_p q_p is split into a product and its
+// exact error (the fma residue) and both are added.  Groups that do not fit
+// (a range of magnitudes beyond 2^14, values below 2^-105, Inf or NaN) take
+// the binary32 path instead for the whole chunk: w = fl(c s + z), then an fma
+// per weight.
 __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -245,6 +259,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // A q4 chunk's share of one lane, read out of the ring stage at once so that
 // the stage can be refilled before the arithmetic starts.  Prep lane
@@ -281,91 +296,285 @@ __device__ __forceinline__ void q4_read(uint32_t st, int lane, int m, Q4Lane<KIN
   }
 }
 
-// One token's x slice (this prep lane's 8 columns) -> byte planes in the
-// warp's scratch; returns the group's sum X_g (g = lane & 7) and sets
-// inv = 2^(E_g - 141).
-__device__ __forceinline__ float q4_x_planes(const uint4 xr, uint32_t scratch, int lane, float& inv) {
-  const int gp = lane & 7, tp = lane >> 3;
+// Scale and zero of row i of this lane's group.
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, float& s, float& z) {
+  if constexpr (KIND == kQ4_1) {
+    s = bf16_bits_to_f32(L.f0[i]);
+    z = bf16_bits_to_f32(L.f1[i]);
+  } else {                                         // exact products: 8 x 6 significant bits
+    s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * static_cast<float>(L.f1[i] & 0xFFFFu);
+    z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
+  }
+}
+
+// Per token, for the lane's group g = lane & 7 (prep and decode lanes of a
+// group share the low three lane bits): the plane weights q_p and the digit
+// sums times them.
+struct XGroup {
+  float q[3];                      // 2^(E-148), 2^(E-140), 2^(E-132)
+  float xq[3];                     // X_p q_p
+};
+
+// Whether one token's x slice is exact in 24-bit fixed point for this lane's
+// group (all four prep lanes of the group get the same answer), and the
+// biased exponent E of the group's largest |x|.
+__device__ __forceinline__ bool q4_x_exact(const uint4 xr, int& E) {
   const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-  uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
-                         __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
+  const uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
+                               __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
   uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+  // smallest nonzero |x| as (binary32 bits << 1) - 1: the sign drops out and
+  // +-0 becomes 0xFFFFFFFF, above every other key
+  uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    mn = min(mn, (xw[j] << 17) - 1u);
+    mn = min(mn, ((xw[j] & 0xFFFF0000u) << 1) - 1u);
+  }
   mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
   mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  const int E = max(static_cast<int>(mx >> 7), 15);             // biased exponent of the group's max |x|
-  const float scale = __int_as_float((268 - E) << 23);          // 2^(141 - E)
-  inv = __int_as_float((E - 14) << 23);                         // 2^(E - 141)
-  float xs = 0.f;
-  int q[8];
+  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 8));
+  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
+  E = static_cast<int>(mx >> 7);
+  const int emin = static_cast<int>((mn + 1u) >> 24);    // exponent field of the smallest nonzero |x|
+  return mx == 0 || (E >= 22 && E <= 254 && emin >= E - 14);
+}
+
+// One token's x slice (this prep lane's 8 columns) -> the three digit planes
+// in the warp's scratch: region A [t][g] 16 B (p0 even, p0 odd, p1 even,
+// p1 odd), region B at +512 [t][g] 8 B (p2 even, p2 odd); and the group's
+// plane weights and digit sums.
+__device__ __forceinline__ void q4_x_planes(const uint4 xr, int E, uint32_t scratch, int lane, XGroup& G) {
+  const int gp = lane & 7, tp = lane >> 3;
+  E = min(max(E, 22), 254);                                      // (an all-zero group: any step)
+  const float sc = __int_as_float((275 - E) << 23);              // 2^(148 - E)
+  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+  uint32_t v[8];                                                 // v + 0x808080 (|v| < 2^22)
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float f0 = __uint_as_float(xw[j] << 16), f1 = __uint_as_float(xw[j] & 0xFFFF0000u);
-    xs += f0 + f1;
-    q[2 * j] = __float_as_int(fmaf(f0, scale, 12582912.0f)) - 0x4B400000;       // round to nearest
-    q[2 * j + 1] = __float_as_int(fmaf(f1, scale, 12582912.0f)) - 0x4B400000;
+    v[2 * j] = __float_as_uint(fmaf(f0, sc, 12582912.0f)) - 0x4ABF7F80u;
+    v[2 * j + 1] = __float_as_uint(fmaf(f1, sc, 12582912.0f)) - 0x4ABF7F80u;
   }
-  xs += __shfl_xor_sync(0xffffffffu, xs, 8);
-  xs += __shfl_xor_sync(0xffffffffu, xs, 16);                   // X_g for g = lane & 7
-  const uint32_t p0e = prmt(prmt(q[0], q[2], 0x0040), prmt(q[4], q[6], 0x0040), 0x5410);
-  const uint32_t p0o = prmt(prmt(q[1], q[3], 0x0040), prmt(q[5], q[7], 0x0040), 0x5410);
-  const uint32_t p1e = prmt(prmt(q[0], q[2], 0x0051), prmt(q[4], q[6], 0x0051), 0x5410);
-  const uint32_t p1o = prmt(prmt(q[1], q[3], 0x0051), prmt(q[5], q[7], 0x0051), 0x5410);
-  // planes of (group gp, word tp) at [tp][gp]: conflict-free both ways
+  // bytes 0..2 of v + 0x808080 are d_p + 128: gather byte p of the even and
+  // of the odd columns, then flip the top bit of each byte to get d_p
+  const uint32_t ae = prmt(v[0], v[2], 0x5140), be = prmt(v[4], v[6], 0x5140);
+  const uint32_t ao = prmt(v[1], v[3], 0x5140), bo = prmt(v[5], v[7], 0x5140);
+  const uint32_t ce = prmt(v[0], v[2], 0x0062), de = prmt(v[4], v[6], 0x0062);
+  const uint32_t co = prmt(v[1], v[3], 0x0062), dq = prmt(v[5], v[7], 0x0062);
+  const uint32_t p0e = prmt(ae, be, 0x5410) ^ 0x80808080u, p0o = prmt(ao, bo, 0x5410) ^ 0x80808080u;
+  const uint32_t p1e = prmt(ae, be, 0x7632) ^ 0x80808080u, p1o = prmt(ao, bo, 0x7632) ^ 0x80808080u;
+  const uint32_t p2e = prmt(ce, de, 0x5410) ^ 0x80808080u, p2o = prmt(co, dq, 0x5410) ^ 0x80808080u;
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(p0e), "r"(p0o),
                "r"(p1e), "r"(p1o)
                : "memory");
-  return xs;
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(scratch + 512 + (tp * 8 + gp) * 8), "r"(p2e), "r"(p2o)
+               : "memory");
+  int X[3];
+  X[0] = dp4a_us(0x01010101u, p0e, dp4a_us(0x01010101u, p0o, 0));
+  X[1] = dp4a_us(0x01010101u, p1e, dp4a_us(0x01010101u, p1o, 0));
+  X[2] = dp4a_us(0x01010101u, p2e, dp4a_us(0x01010101u, p2o, 0));
+#pragma unroll
+  for (int p = 0; p < 3; ++p) {
+    X[p] += __shfl_xor_sync(0xffffffffu, X[p], 8);
+    X[p] += __shfl_xor_sync(0xffffffffu, X[p], 16);              // X_p of group gp
+    G.q[p] = __int_as_float((E - 21 + 8 * p) << 23);              // 2^(E - 148 + 8p)
+    G.xq[p] = static_cast<float>(X[p]) * G.q[p];                  // exact: |X_p| <= 4096
+  }
+}
+
+// One token's planes of this lane's group against two rows' codes: the
+// per-plane partials added to (acc.x, acc.y).
+template <int KIND>
+__device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uint32_t (&hi)[2][4], float2 s2,
+                                           float2 z2, const uint4 (&PA)[4], const uint2 (&PB)[4], const XGroup& G,
+                                           float2 acc) {
+  int S[2][3];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    int a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      a0 = dp4a_us(lo[r][t], PA[t].x, a0);
+      a0 = dp4a_us(hi[r][t], PA[t].y, a0);
+      a1 = dp4a_us(lo[r][t], PA[t].z, a1);
+      a1 = dp4a_us(hi[r][t], PA[t].w, a1);
+      a2 = dp4a_us(lo[r][t], PB[t].x, a2);
+      a2 = dp4a_us(hi[r][t], PB[t].y, a2);
+    }
+    S[r][0] = a0;
+    S[r][1] = a1;
+    S[r][2] = a2;
+  }
+#pragma unroll
+  for (int p = 2; p >= 0; --p) {
+    const float2 qq = make_float2(G.q[p], G.q[p]);
+    const float2 xq = make_float2(G.xq[p], G.xq[p]);
+    // exact: |S_p| < 2^24 times a power of two
+    const float2 sq = fmul2(make_float2(__int2float_rn(S[0][p]), __int2float_rn(S[1][p])), qq);
+    if constexpr (KIND == kQ4_1) {
+      const float2 zx = fmul2(z2, xq);                          // exact: 8 x 13 significant bits
+      acc = fadd2(acc, ffma2(s2, sq, zx));
+    } else {
+      const float2 zx = fmul2(z2, xq);                          // rounded; its error added below
+      const float2 ze = ffma2(z2, xq, make_float2(-zx.x, -zx.y));
+      acc = fadd2(fadd2(acc, ffma2(s2, sq, zx)), ze);
+    }
+  }
+  return acc;
+}
+
+// The exact-integer path for one chunk: rows 4i + qr of group g, every token.
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
+                                         const XGroup (&G)[MT], float (&yacc)[MT][8]) {
+  const int g = lane & 7;
+  if constexpr (MT == 1) {
+    uint4 PA[4];
+    uint2 PB[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      PA[t] = lds128(scratch + (t * 8 + g) * 16);
+      PB[t] = lds64(scratch + 512 + (t * 8 + g) * 8);
+    }
+    __syncwarp();                                               // scratch is rewritten by the next chunk
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {                            // rows 4i + qr and 4(i+1) + qr, paired
+      float s[2], z[2];
+      uint32_t lo[2][4], hi[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        q4_scale_zero(L, i + r, s[r], z[r]);
+        const uint32_t w[4] = {L.cw[i + r].x, L.cw[i + r].y, L.cw[i + r].z, L.cw[i + r].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          lo[r][t] = w[t] & 0x0F0F0F0Fu;
+          hi[r][t] = (w[t] >> 4) & 0x0F0F0F0Fu;
+        }
+      }
+      const float2 acc = q4_rows2<KIND>(lo, hi, make_float2(s[0], s[1]), make_float2(z[0], z[1]), PA, PB, G[0],
+                                        make_float2(yacc[0][i], yacc[0][i + 1]));
+      yacc[0][i] = acc.x;
+      yacc[0][i + 1] = acc.y;
+    }
+  } else {
+    // several tokens: the codes are unpacked once for all rows, the planes
+    // are read one token at a time
+    uint32_t lo[4][2][4], hi[4][2][4];
+    float2 s2[4], z2[4];
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip) {
+      float s[2], z[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        q4_scale_zero(L, 2 * ip + r, s[r], z[r]);
+        const uint32_t w[4] = {L.cw[2 * ip + r].x, L.cw[2 * ip + r].y, L.cw[2 * ip + r].z, L.cw[2 * ip + r].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          lo[ip][r][t] = w[t] & 0x0F0F0F0Fu;
+          hi[ip][r][t] = (w[t] >> 4) & 0x0F0F0F0Fu;
+        }
+      }
+      s2[ip] = make_float2(s[0], s[1]);
+      z2[ip] = make_float2(z[0], z[1]);
+    }
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok) {
+      if (tok >= m) break;
+      uint4 PA[4];
+      uint2 PB[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        PA[t] = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
+        PB[t] = lds64(scratch + tok * kScratchBytes + 512 + (t * 8 + g) * 8);
+      }
+#pragma unroll
+      for (int ip = 0; ip < 4; ++ip) {
+        const float2 acc = q4_rows2<KIND>(lo[ip], hi[ip], s2[ip], z2[ip], PA, PB, G[tok],
+                                          make_float2(yacc[tok][2 * ip], yacc[tok][2 * ip + 1]));
+        yacc[tok][2 * ip] = acc.x;
+        yacc[tok][2 * ip + 1] = acc.y;
+      }
+    }
+    __syncwarp();                                               // scratch is rewritten by the next chunk
+  }
+}
+
+// The binary32 path for one chunk (x groups that 24-bit fixed point does not
+// hold): every weight formed as fl(c s + z) and multiplied by x in an fma.
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
+                                         float (&yacc)[MT][8]) {
+  const int g = lane & 7;
+  const float2 magic = make_float2(-8388608.0f, -8388608.0f);   // 2^23: float(2^23 + c) - 2^23 = c exactly
+#pragma unroll 1
+  for (int tok = 0; tok < m; ++tok) {
+    float2 xf[16];                                              // columns 2j, 2j + 1 of group g
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 xw = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
+      const uint32_t w[4] = {xw.x, xw.y, xw.z, xw.w};
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        xf[4 * t + b] = make_float2(__uint_as_float(w[b] << 16), __uint_as_float(w[b] & 0xFFFF0000u));
+    }
+    float part[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float s, z;
+      q4_scale_zero(L, i, s, z);
+      const float2 s2 = make_float2(s, s), z2 = make_float2(z, z);
+      const uint32_t w[4] = {L.cw[i].x, L.cw[i].y, L.cw[i].z, L.cw[i].w};
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t lo = w[t] & 0x0F0F0F0Fu, hi = (w[t] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float2 c = fadd2(make_float2(__uint_as_float(prmt(lo, 0x4B000000u, 0x7540 + b)),
+                                             __uint_as_float(prmt(hi, 0x4B000000u, 0x7540 + b))), magic);
+          acc = ffma2(ffma2(c, s2, z2), xf[4 * t + b], acc);
+        }
+      }
+      part[i] = acc.x + acc.y;
+    }
+    // (tok is a loop variable: select the token's accumulators by comparison,
+    // so that they stay in registers)
+#pragma unroll
+    for (int u = 0; u < MT; ++u)
+      if (u == tok)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) yacc[u][i] += part[i];
+  }
+  __syncwarp();                                                 // scratch is rewritten by the next chunk
 }
 
 template <int KIND, int MT>
 __device__ __forceinline__ void q4_compute(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
                                            float (&yacc)[MT][8]) {
-  float xs[MT], inv[MT];
+  int E[MT];
+  bool exact = true;
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok)
-    if (tok < m) xs[tok] = q4_x_planes(L.xr[tok], scratch + tok * kScratchBytes, lane, inv[tok]);
-  __syncwarp();
-  // ---- decode lane: rows 4i + qr of group g; every token's planes at hand
-  const int g = lane & 7;
-  uint4 P[MT][4];
+    if (tok < m) exact &= q4_x_exact(L.xr[tok], E[tok]);
+  if (__all_sync(0xffffffffu, exact)) {
+    XGroup G[MT];
 #pragma unroll
-  for (int tok = 0; tok < MT; ++tok)
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) q4_x_planes(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
+    __syncwarp();
+    q4_fixed<KIND, MT>(L, scratch, lane, m, G, yacc);
+  } else {
+    const int gp = lane & 7, tp = lane >> 3;
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (tok < m) P[tok][t] = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
-  __syncwarp();                                                 // scratch is rewritten by the next chunk
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float s, z;
-    if constexpr (KIND == kQ4_1) {
-      s = bf16_bits_to_f32(L.f0[i]);
-      z = bf16_bits_to_f32(L.f1[i]);
-    } else {
-      s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * static_cast<float>(L.f1[i] & 0xFFFFu);
-      z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
-    }
-    const uint32_t w[4] = {L.cw[i].x, L.cw[i].y, L.cw[i].z, L.cw[i].w};
-    uint32_t lo[4], hi[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      lo[t] = w[t] & 0x0F0F0F0Fu;
-      hi[t] = (w[t] >> 4) & 0x0F0F0F0Fu;
-    }
-#pragma unroll
-    for (int tok = 0; tok < MT; ++tok) {
-      if (tok >= m) break;
-      uint32_t s0 = 0;
-      int s1 = 0;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        s0 = dp4a_uu(lo[t], P[tok][t].x, s0);
-        s0 = dp4a_uu(hi[t], P[tok][t].y, s0);
-        s1 = dp4a_us(lo[t], P[tok][t].z, s1);
-        s1 = dp4a_us(hi[t], P[tok][t].w, s1);
-      }
-      const float dot = __int2float_rn(s1 * 256 + static_cast<int>(s0));   // exact: |.| < 2^24
-      yacc[tok][i] = fmaf(s * inv[tok], dot, fmaf(z, xs[tok], yacc[tok][i]));
-    }
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + tok * kScratchBytes + (tp * 8 + gp) * 16),
+                     "r"(L.xr[tok].x), "r"(L.xr[tok].y), "r"(L.xr[tok].z), "r"(L.xr[tok].w)
+                     : "memory");
+    __syncwarp();
+    q4_float<KIND, MT>(L, scratch, lane, m, yacc);
   }
 }
 
@@ -542,12 +751,12 @@ __device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, in
 
 // Threads per CTA the kernel is compiled for.  One token: at most 128
 // registers, so that two CTAs of 8 warps share an SM (consecutive launches
-// overlap).  Two tokens of a 4-bit kind: 12 warps, the most that the tokens'
-// registers allow, to hide the latency of the integer dot products.
-// Otherwise 8 warps with the register budget of a lone CTA.
+// overlap).  Several tokens: 8 warps with the register budget of a lone CTA
+// (two warps per SM sub-partition: up to 255 registers; three would cap them
+// at 168, below what the tokens' digit planes and unpacked codes need).
 template <int KIND, int MT>
 constexpr int gemv_max_threads() {
-  return MT == 1 ? 512 : (MT == 2 && (KIND == kQ4_1 || KIND == kQ4_K)) ? 384 : 256;
+  return MT == 1 ? 512 : 256;
 }
 
 template <int KIND, int MAXB, int MT>
@@ -687,8 +896,9 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
 constexpr int kTwoCtaChunksPerSm = 128;
 
 static int gemv_max_warps(int kind, int MT) {
-  const bool q4 = kind == kQ4_1 || kind == kQ4_K;
-  return MT == 1 ? 8 : (MT == 2 && q4) ? 12 : 8;
+  (void)kind;
+  (void)MT;
+  return 8;
 }
 
 bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT) {

@@ -114,6 +114,41 @@ def activations(g: np.random.Generator, M: int, K: int, sigma: float = 1.0) -> n
     return bf16_bits(g.normal(0.0, sigma, size=(M, K)))
 
 
+def activations_outliers(g: np.random.Generator, M: int, K: int, frac: float = 0.005, lo: float = 100.0,
+                         hi: float = 1000.0) -> np.ndarray:
+    """bf16 bits [M, K]: N(0, 1) with a fixed set of outlier channels (a fraction
+    `frac` of the columns, at least one) scaled by U(lo, hi), the way a few
+    channels of LLM hidden states run 10^2 - 10^3 times the rest."""
+    x = g.normal(0.0, 1.0, size=(M, K))
+    n = max(1, int(round(frac * K)))
+    cols = g.choice(K, size=n, replace=False)
+    x[:, cols] *= g.uniform(lo, hi, size=n)
+    return bf16_bits(x)
+
+
+def activations_log_uniform(g: np.random.Generator, M: int, K: int, lo_exp: float = -30.0,
+                            hi_exp: float = 30.0, zero_frac: float = 0.05) -> np.ndarray:
+    """bf16 bits [M, K]: random signs, magnitudes 2^U(lo_exp, hi_exp), a fraction
+    of exact zeros (both signs): groups whose magnitudes span far more than
+    any fixed-point width."""
+    mag = np.exp2(g.uniform(lo_exp, hi_exp, size=(M, K)))
+    x = np.where(g.random((M, K)) < 0.5, -mag, mag)
+    z = g.random((M, K)) < zero_frac
+    x[z] = np.where(g.random(int(z.sum())) < 0.5, -0.0, 0.0)
+    return bf16_bits(x)
+
+
+def activations_subnormal(g: np.random.Generator, M: int, K: int, zero_frac: float = 0.3) -> np.ndarray:
+    """bf16 bits [M, K]: bf16 subnormals (exponent field 0, random nonzero
+    mantissa and sign) mixed with +0 and -0."""
+    mant = g.integers(1, 128, size=(M, K), dtype=np.uint16)
+    sign = (g.random((M, K)) < 0.5).astype(np.uint16) << 15
+    bits = sign | mant
+    z = g.random((M, K)) < zero_frac
+    bits[z] = sign[z]
+    return bits
+
+
 # --------------------------------------------------------------------------
 # writers: logical fields -> chunk bytes
 # --------------------------------------------------------------------------
