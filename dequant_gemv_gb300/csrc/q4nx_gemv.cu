@@ -39,7 +39,7 @@
 namespace q4nx {
 
 constexpr int kXSliceBytes = 512;            // bf16 x of one tile column, per token
-constexpr int kScratchBytes = 768;           // per warp and token: x digit planes (or the raw x slice) of one chunk
+constexpr int kScratchBytes = 1024;          // per warp and token: x digit planes (or the raw x slice) of one chunk
 constexpr int kSlotBytes = 2 * 32 * 4;       // per warp and token: sums of its first and last tile row
 constexpr int kCntBytes = 8;                 // per warp: arrival counters of its first and last tile row
 constexpr int kMaxBatch = kMaxGemvItems;
@@ -61,6 +61,7 @@ struct GemvArgsT {
   int nitems;
   int grid;                // CTAs; CTA b owns chunks [T b / grid, T (b+1) / grid)
   int stages;
+  int xslots;              // 4-bit kinds, one token: x-slice cache slots in shared memory (0: none)
   int out_f32;
   int m;                   // tokens (1 unless one item against several tokens)
   int64_t x_stride;        // bytes between tokens' x
@@ -88,6 +89,24 @@ __shared__ unsigned long long s_top1_key;
 constexpr int kMaxGemvWarps = 16;          // warps per CTA the plan may choose (12 at most today)
 __shared__ uint32_t s_wlo[kMaxGemvWarps];
 __shared__ long long s_clast;
+
+// x-slice cache (4-bit kinds, one token).  Every warp used to turn the x
+// slice of each chunk it read into digit planes, although the chunks of one
+// tile column share the slice: with a CTA's range spanning several tile rows,
+// that preparation was repeated for every row (a fifth of the arithmetic).
+// A CTA whose chunks touch at most kXTabItems items and as many (item, tile
+// column) slices as the launch's cache slots holds prepares each slice once,
+// after the wait on the previous grid, into a 1280-byte slot: regions A and B
+// (512 B each) as in a warp's scratch, or the raw bf16 slice when the slice
+// needs the binary32 path; then per group 32 B: q0, xq0..xq3 and the slice's
+// mode (3 or 4 digit planes, 5 for binary32).  Slots of one item are its
+// touched tile columns in order, starting from column tc0 and wrapping.
+constexpr int kXSlotBytes = 1280;
+constexpr int kXSlotG = 1024;              // per-group records within a slot
+constexpr int kXTabItems = 16;
+constexpr int kMaxXSlots = 32;
+__shared__ int4 s_xtab[kXTabItems];        // per touched item: {first slot, tc0, slots, TC}
+__shared__ int s_xinfo[4];                 // cache used (0/1), first touched item, slots in use, items touched
 
 // Lane-wise transpose-reduce of 8 values over the 8 lanes selected by masks
 // (m2, m1, m0): afterwards the lane whose mask bits read (b2 b1 b0) holds the
@@ -275,12 +294,13 @@ struct Q4Lane {
 };
 
 template <int KIND, int MT>
-__device__ __forceinline__ void q4_read(uint32_t st, int lane, int m, Q4Lane<KIND, MT>& L) {
-  constexpr int CB = chunk_bytes_of(KIND);
+__device__ __forceinline__ void q4_read(uint32_t st, uint32_t xs, bool with_x, int lane, int m, Q4Lane<KIND, MT>& L) {
   const int gp = lane & 7, tp = lane >> 3;
+  if (with_x) {
 #pragma unroll
-  for (int tok = 0; tok < MT; ++tok)
-    if (tok < m) L.xr[tok] = lds128(st + CB + tok * kXSliceBytes + gp * 64 + tp * 16);
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) L.xr[tok] = lds128(xs + tok * kXSliceBytes + gp * 64 + tp * 16);
+  }
   const int qr = lane >> 3, g = lane & 7;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -309,17 +329,20 @@ __device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, 
 }
 
 // Per token, for the lane's group g = lane & 7 (prep and decode lanes of a
-// group share the low three lane bits): the plane weights q_p and the digit
-// sums times them.
+// group share the low three lane bits): the weight of the lowest digit plane
+// and the digit sums times the plane weights.
 struct XGroup {
-  float q[3];                      // 2^(E-148), 2^(E-140), 2^(E-132)
-  float xq[3];                     // X_p q_p
+  float q0;                        // 2^(E - 124 - 8 NP); plane p weighs q0 256^p
+  float xq[4];                     // X_p q0 256^p
 };
 
-// Whether one token's x slice is exact in 24-bit fixed point for this lane's
-// group (all four prep lanes of the group get the same answer), and the
-// biased exponent E of the group's largest |x|.
-__device__ __forceinline__ bool q4_x_exact(const uint4 xr, int& E) {
+// How many digit planes one token's x slice needs for this lane's group (all
+// four prep lanes of the group get the same answer): 3 when every value is a
+// multiple of 2^(E-148) below 2^(E-126) (E the biased exponent of the group's
+// largest |x|: nonzero values within 2^14 of the largest, 22 <= E <= 254), 4
+// when within 2^22 (30 <= E <= 254, step 2^(E-156)), else 5 (none does: the
+// binary32 path).  An all-zero group needs 3.
+__device__ __forceinline__ int q4_x_need(const uint4 xr, int& E) {
   const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
   const uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
                                __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
@@ -338,62 +361,75 @@ __device__ __forceinline__ bool q4_x_exact(const uint4 xr, int& E) {
   mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
   E = static_cast<int>(mx >> 7);
   const int emin = static_cast<int>((mn + 1u) >> 24);    // exponent field of the smallest nonzero |x|
-  return mx == 0 || (E >= 22 && E <= 254 && emin >= E - 14);
+  if (mx == 0 || (E >= 22 && E <= 254 && emin >= E - 14)) return 3;
+  if (E >= 30 && E <= 254 && emin >= E - 22) return 4;
+  return 5;
 }
 
-// One token's x slice (this prep lane's 8 columns) -> the three digit planes
-// in the warp's scratch: region A [t][g] 16 B (p0 even, p0 odd, p1 even,
-// p1 odd), region B at +512 [t][g] 8 B (p2 even, p2 odd); and the group's
-// plane weights and digit sums.
+// One token's x slice (this prep lane's 8 columns) -> NP digit planes in
+// `scratch`: region A [t][g] 16 B (p0 even, p0 odd, p1 even, p1 odd) and
+// region B at +512 [t][g] 16 B (p2 even, p2 odd, p3 even, p3 odd); and the
+// group's plane weight and digit sums.  v_k = x_k 2^(124 + 8 NP - E), |v_k| <
+// 2^(8 NP - 2), exact by q4_x_need; v_k + 0x80..80 has the bytes d_p + 128.
+template <int NP>
 __device__ __forceinline__ void q4_x_planes(const uint4 xr, int E, uint32_t scratch, int lane, XGroup& G) {
   const int gp = lane & 7, tp = lane >> 3;
-  E = min(max(E, 22), 254);                                      // (an all-zero group: any step)
-  const float sc = __int_as_float((275 - E) << 23);              // 2^(148 - E)
+  E = min(max(E, 8 * NP - 2), 254);                              // (an all-zero group: any step)
+  const float sc = __int_as_float((251 + 8 * NP - E) << 23);     // 2^(124 + 8 NP - E)
   const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-  uint32_t v[8];                                                 // v + 0x808080 (|v| < 2^22)
+  uint32_t v[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float f0 = __uint_as_float(xw[j] << 16), f1 = __uint_as_float(xw[j] & 0xFFFF0000u);
-    v[2 * j] = __float_as_uint(fmaf(f0, sc, 12582912.0f)) - 0x4ABF7F80u;
-    v[2 * j + 1] = __float_as_uint(fmaf(f1, sc, 12582912.0f)) - 0x4ABF7F80u;
+    if constexpr (NP == 3) {                                     // |v| < 2^22: round by the 1.5 * 2^23 magic number
+      v[2 * j] = __float_as_uint(fmaf(f0, sc, 12582912.0f)) - 0x4ABF7F80u;
+      v[2 * j + 1] = __float_as_uint(fmaf(f1, sc, 12582912.0f)) - 0x4ABF7F80u;
+    } else {                                                     // |v| < 2^30: an integer conversion
+      v[2 * j] = static_cast<uint32_t>(__float2int_rn(f0 * sc)) + 0x80808080u;
+      v[2 * j + 1] = static_cast<uint32_t>(__float2int_rn(f1 * sc)) + 0x80808080u;
+    }
   }
-  // bytes 0..2 of v + 0x808080 are d_p + 128: gather byte p of the even and
-  // of the odd columns, then flip the top bit of each byte to get d_p
+  // gather byte p of the even and of the odd columns, then flip the top bit
+  // of each byte to get d_p
   const uint32_t ae = prmt(v[0], v[2], 0x5140), be = prmt(v[4], v[6], 0x5140);
   const uint32_t ao = prmt(v[1], v[3], 0x5140), bo = prmt(v[5], v[7], 0x5140);
-  const uint32_t ce = prmt(v[0], v[2], 0x0062), de = prmt(v[4], v[6], 0x0062);
-  const uint32_t co = prmt(v[1], v[3], 0x0062), dq = prmt(v[5], v[7], 0x0062);
-  const uint32_t p0e = prmt(ae, be, 0x5410) ^ 0x80808080u, p0o = prmt(ao, bo, 0x5410) ^ 0x80808080u;
-  const uint32_t p1e = prmt(ae, be, 0x7632) ^ 0x80808080u, p1o = prmt(ao, bo, 0x7632) ^ 0x80808080u;
-  const uint32_t p2e = prmt(ce, de, 0x5410) ^ 0x80808080u, p2o = prmt(co, dq, 0x5410) ^ 0x80808080u;
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(p0e), "r"(p0o),
-               "r"(p1e), "r"(p1o)
+  const uint32_t ce = prmt(v[0], v[2], 0x7362), de = prmt(v[4], v[6], 0x7362);
+  const uint32_t co = prmt(v[1], v[3], 0x7362), dq = prmt(v[5], v[7], 0x7362);
+  uint32_t P[4][2];
+  P[0][0] = prmt(ae, be, 0x5410) ^ 0x80808080u;
+  P[0][1] = prmt(ao, bo, 0x5410) ^ 0x80808080u;
+  P[1][0] = prmt(ae, be, 0x7632) ^ 0x80808080u;
+  P[1][1] = prmt(ao, bo, 0x7632) ^ 0x80808080u;
+  P[2][0] = prmt(ce, de, 0x5410) ^ 0x80808080u;
+  P[2][1] = prmt(co, dq, 0x5410) ^ 0x80808080u;
+  P[3][0] = NP == 4 ? prmt(ce, de, 0x7632) ^ 0x80808080u : 0u;
+  P[3][1] = NP == 4 ? prmt(co, dq, 0x7632) ^ 0x80808080u : 0u;
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(P[0][0]),
+               "r"(P[0][1]), "r"(P[1][0]), "r"(P[1][1])
                : "memory");
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(scratch + 512 + (tp * 8 + gp) * 8), "r"(p2e), "r"(p2o)
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + 512 + (tp * 8 + gp) * 16), "r"(P[2][0]),
+               "r"(P[2][1]), "r"(P[3][0]), "r"(P[3][1])
                : "memory");
-  int X[3];
-  X[0] = dp4a_us(0x01010101u, p0e, dp4a_us(0x01010101u, p0o, 0));
-  X[1] = dp4a_us(0x01010101u, p1e, dp4a_us(0x01010101u, p1o, 0));
-  X[2] = dp4a_us(0x01010101u, p2e, dp4a_us(0x01010101u, p2o, 0));
+  G.q0 = __int_as_float((E + 3 - 8 * NP) << 23);                 // 2^(E - 124 - 8 NP)
 #pragma unroll
-  for (int p = 0; p < 3; ++p) {
-    X[p] += __shfl_xor_sync(0xffffffffu, X[p], 8);
-    X[p] += __shfl_xor_sync(0xffffffffu, X[p], 16);              // X_p of group gp
-    G.q[p] = __int_as_float((E - 21 + 8 * p) << 23);              // 2^(E - 148 + 8p)
-    G.xq[p] = static_cast<float>(X[p]) * G.q[p];                  // exact: |X_p| <= 4096
+  for (int p = 0; p < NP; ++p) {
+    int X = dp4a_us(0x01010101u, P[p][0], dp4a_us(0x01010101u, P[p][1], 0));
+    X += __shfl_xor_sync(0xffffffffu, X, 8);
+    X += __shfl_xor_sync(0xffffffffu, X, 16);                    // X_p of group gp (|X_p| <= 4096)
+    G.xq[p] = static_cast<float>(X) * __int_as_float((E + 3 - 8 * NP + 8 * p) << 23);   // exact
   }
 }
 
 // One token's planes of this lane's group against two rows' codes: the
 // per-plane partials added to (acc.x, acc.y).
-template <int KIND>
+template <int KIND, int NP>
 __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uint32_t (&hi)[2][4], float2 s2,
-                                           float2 z2, const uint4 (&PA)[4], const uint2 (&PB)[4], const XGroup& G,
+                                           float2 z2, const uint4 (&PA)[4], const uint4 (&PB)[4], const XGroup& G,
                                            float2 acc) {
-  int S[2][3];
+  int S[2][4];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    int a0 = 0, a1 = 0, a2 = 0;
+    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       a0 = dp4a_us(lo[r][t], PA[t].x, a0);
@@ -402,14 +438,20 @@ __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uin
       a1 = dp4a_us(hi[r][t], PA[t].w, a1);
       a2 = dp4a_us(lo[r][t], PB[t].x, a2);
       a2 = dp4a_us(hi[r][t], PB[t].y, a2);
+      if constexpr (NP == 4) {
+        a3 = dp4a_us(lo[r][t], PB[t].z, a3);
+        a3 = dp4a_us(hi[r][t], PB[t].w, a3);
+      }
     }
     S[r][0] = a0;
     S[r][1] = a1;
     S[r][2] = a2;
+    S[r][3] = a3;
   }
 #pragma unroll
-  for (int p = 2; p >= 0; --p) {
-    const float2 qq = make_float2(G.q[p], G.q[p]);
+  for (int p = NP - 1; p >= 0; --p) {
+    const float qp = G.q0 * static_cast<float>(1 << (8 * p));        // exact power of two
+    const float2 qq = make_float2(qp, qp);
     const float2 xq = make_float2(G.xq[p], G.xq[p]);
     // exact: |S_p| < 2^24 times a power of two
     const float2 sq = fmul2(make_float2(__int2float_rn(S[0][p]), __int2float_rn(S[1][p])), qq);
@@ -425,20 +467,27 @@ __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uin
   return acc;
 }
 
-// The exact-integer path for one chunk: rows 4i + qr of group g, every token.
-template <int KIND, int MT>
+// The exact-integer path for one chunk: rows 4i + qr of group g, every token,
+// NP digit planes per token in `scratch` (token stride kScratchBytes).
+template <int KIND, int MT, int NP>
 __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
                                          const XGroup (&G)[MT], float (&yacc)[MT][8]) {
   const int g = lane & 7;
-  if constexpr (MT == 1) {
-    uint4 PA[4];
-    uint2 PB[4];
+  auto load_planes = [&](int tok, uint4 (&PA)[4], uint4 (&PB)[4]) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      PA[t] = lds128(scratch + (t * 8 + g) * 16);
-      PB[t] = lds64(scratch + 512 + (t * 8 + g) * 8);
+      PA[t] = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
+      if constexpr (NP == 4) {
+        PB[t] = lds128(scratch + tok * kScratchBytes + 512 + (t * 8 + g) * 16);
+      } else {
+        const uint2 b2 = lds64(scratch + tok * kScratchBytes + 512 + (t * 8 + g) * 16);
+        PB[t] = make_uint4(b2.x, b2.y, 0u, 0u);
+      }
     }
-    __syncwarp();                                               // scratch is rewritten by the next chunk
+  };
+  if constexpr (MT == 1) {
+    uint4 PA[4], PB[4];
+    load_planes(0, PA, PB);
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {                            // rows 4i + qr and 4(i+1) + qr, paired
       float s[2], z[2];
@@ -453,8 +502,8 @@ __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scr
           hi[r][t] = (w[t] >> 4) & 0x0F0F0F0Fu;
         }
       }
-      const float2 acc = q4_rows2<KIND>(lo, hi, make_float2(s[0], s[1]), make_float2(z[0], z[1]), PA, PB, G[0],
-                                        make_float2(yacc[0][i], yacc[0][i + 1]));
+      const float2 acc = q4_rows2<KIND, NP>(lo, hi, make_float2(s[0], s[1]), make_float2(z[0], z[1]), PA, PB, G[0],
+                                            make_float2(yacc[0][i], yacc[0][i + 1]));
       yacc[0][i] = acc.x;
       yacc[0][i + 1] = acc.y;
     }
@@ -482,27 +531,23 @@ __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scr
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok) {
       if (tok >= m) break;
-      uint4 PA[4];
-      uint2 PB[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        PA[t] = lds128(scratch + tok * kScratchBytes + (t * 8 + g) * 16);
-        PB[t] = lds64(scratch + tok * kScratchBytes + 512 + (t * 8 + g) * 8);
-      }
+      uint4 PA[4], PB[4];
+      load_planes(tok, PA, PB);
 #pragma unroll
       for (int ip = 0; ip < 4; ++ip) {
-        const float2 acc = q4_rows2<KIND>(lo[ip], hi[ip], s2[ip], z2[ip], PA, PB, G[tok],
-                                          make_float2(yacc[tok][2 * ip], yacc[tok][2 * ip + 1]));
+        const float2 acc = q4_rows2<KIND, NP>(lo[ip], hi[ip], s2[ip], z2[ip], PA, PB, G[tok],
+                                              make_float2(yacc[tok][2 * ip], yacc[tok][2 * ip + 1]));
         yacc[tok][2 * ip] = acc.x;
         yacc[tok][2 * ip + 1] = acc.y;
       }
     }
-    __syncwarp();                                               // scratch is rewritten by the next chunk
   }
+  __syncwarp();                                                 // scratch is rewritten by the next chunk
 }
 
-// The binary32 path for one chunk (x groups that 24-bit fixed point does not
+// The binary32 path for one chunk (x groups that 32-bit fixed point does not
 // hold): every weight formed as fl(c s + z) and multiplied by x in an fma.
+// The raw bf16 x slices are in region A of `scratch`, [t][g] 16 B.
 template <int KIND, int MT>
 __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
                                          float (&yacc)[MT][8]) {
@@ -550,21 +595,32 @@ __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scr
   __syncwarp();                                                 // scratch is rewritten by the next chunk
 }
 
+// One chunk, x prepared here: each token's slice becomes digit planes in the
+// warp's scratch (3 or 4 planes, the most any token's groups need), or, when
+// some group spans more than 32-bit fixed point holds, the raw slices go to
+// the scratch for the binary32 path.
 template <int KIND, int MT>
 __device__ __forceinline__ void q4_compute(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
                                            float (&yacc)[MT][8]) {
   int E[MT];
-  bool exact = true;
+  int need = 3;
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok)
-    if (tok < m) exact &= q4_x_exact(L.xr[tok], E[tok]);
-  if (__all_sync(0xffffffffu, exact)) {
-    XGroup G[MT];
+    if (tok < m) need = max(need, q4_x_need(L.xr[tok], E[tok]));
+  need = __reduce_max_sync(0xffffffffu, need);
+  XGroup G[MT];
+  if (need == 3) {
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok)
-      if (tok < m) q4_x_planes(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
+      if (tok < m) q4_x_planes<3>(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
     __syncwarp();
-    q4_fixed<KIND, MT>(L, scratch, lane, m, G, yacc);
+    q4_fixed<KIND, MT, 3>(L, scratch, lane, m, G, yacc);
+  } else if (need == 4) {
+#pragma unroll
+    for (int tok = 0; tok < MT; ++tok)
+      if (tok < m) q4_x_planes<4>(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
+    __syncwarp();
+    q4_fixed<KIND, MT, 4>(L, scratch, lane, m, G, yacc);
   } else {
     const int gp = lane & 7, tp = lane >> 3;
 #pragma unroll
@@ -586,7 +642,7 @@ __device__ __forceinline__ void q8_lane_map(int lane, int& qe, int& kc) {
 }
 
 template <int KIND, int MT>
-__device__ __forceinline__ void q8_chunk(uint32_t st, int lane, int m, float (&yacc)[MT][8]) {
+__device__ __forceinline__ void q8_chunk(uint32_t st, uint32_t xs, int lane, int m, float (&yacc)[MT][8]) {
   int qe, kc;
   q8_lane_map<KIND>(lane, qe, kc);
   const float MAGIC = 8388736.0f;   // 2^23 + 128: float(2^23 + (c ^ 0x80)) - MAGIC == c exactly
@@ -617,7 +673,7 @@ __device__ __forceinline__ void q8_chunk(uint32_t st, int lane, int m, float (&y
 #pragma unroll
       for (int tok = 0; tok < MT; ++tok) {
         if (tok >= m) break;
-        const float xk = bf16_bits_to_f32(lds_u16(st + kQ8Bytes + tok * kXSliceBytes + (g * 32 + kk) * 2));
+        const float xk = bf16_bits_to_f32(lds_u16(xs + tok * kXSliceBytes + (g * 32 + kk) * 2));
         const float2 xx = make_float2(xk, xk);
         acc[tok][0] = ffma2(c01, xx, acc[tok][0]);
         acc[tok][1] = ffma2(c23, xx, acc[tok][1]);
@@ -734,19 +790,63 @@ __device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_
   }
 }
 
+// A stage's copies complete on its barrier: the chunk, plus `xbytes` of x
+// slices (0 when the CTA's x-slice cache serves the chunk).
 template <int KIND, int MT, class GemvArgs>
-__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
+__device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, uint32_t xbytes, uint8_t* dst,
+                                            uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  mbar_arrive_expect_tx(bar, CB + m * kXSliceBytes);
+  mbar_arrive_expect_tx(bar, CB + xbytes);
   bulk_g2s(dst, a.items[p.it].chunks + p.local * CB, CB, bar);
 }
 template <int KIND, int MT, class GemvArgs>
 __device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
-  constexpr int CB = chunk_bytes_of(KIND);
   const uint8_t* x = a.items[p.it].x + static_cast<int64_t>(p.tc) * kXSliceBytes;
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok)
-    if (tok < m) bulk_g2s(dst + CB + tok * kXSliceBytes, x + tok * a.x_stride, kXSliceBytes, bar);
+    if (tok < m) bulk_g2s(dst + tok * kXSliceBytes, x + tok * a.x_stride, kXSliceBytes, bar);
+}
+
+// The cache slot of the chunk at position p (the CTA caches x slices).
+__device__ __forceinline__ int xslot_of(const Pos& p) {
+  const int4 e = s_xtab[p.it - s_xinfo[1]];
+  int d = p.tc - e.y;
+  if (d < 0) d += e.w;
+  return e.x + d;
+}
+
+__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// One x slice (its bf16 values in this prep lane's xr) into cache slot `sa`:
+// 3 or 4 digit planes (the most any of its groups needs), or the raw slice
+// for the binary32 path; the group records hold q0, xq0..xq3 and that mode.
+__device__ __forceinline__ void xslot_fill(const uint4 xr, uint32_t sa, int lane) {
+  const int gp = lane & 7, tp = lane >> 3;
+  int E;
+  const int need = __reduce_max_sync(0xffffffffu, q4_x_need(xr, E));
+  XGroup G = {};
+  if (need == 3) {
+    q4_x_planes<3>(xr, E, sa, lane, G);
+  } else if (need == 4) {
+    q4_x_planes<4>(xr, E, sa, lane, G);
+  } else {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sa + (tp * 8 + gp) * 16), "r"(xr.x), "r"(xr.y),
+                 "r"(xr.z), "r"(xr.w)
+                 : "memory");
+  }
+  if (tp == 0) {
+    const uint32_t gr = sa + kXSlotG + gp * 32;
+    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(gr), "f"(G.q0), "f"(G.xq[0]), "f"(G.xq[1]),
+                 "f"(G.xq[2])
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(gr + 16), "r"(__float_as_uint(G.xq[3])),
+                 "r"(static_cast<uint32_t>(need)), "r"(0u), "r"(0u)
+                 : "memory");
+  }
 }
 
 // Threads per CTA the kernel is compiled for.  One token: at most 128
@@ -762,8 +862,9 @@ constexpr int gemv_max_threads() {
 template <int KIND, int MAXB, int MT>
 __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int SB = chunk_bytes_of(KIND) + MT * kXSliceBytes;     // stage bytes
+  constexpr int CB = chunk_bytes_of(KIND);                         // a ring stage holds one chunk
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
+  constexpr bool XC = Q4 && MT == 1;                               // may use the x-slice cache
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int m = (MT == 1) ? 1 : a.m;
@@ -771,13 +872,19 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   const int64_t Lc = (a.T * b) / a.grid, Hc = (a.T * (b + 1)) / a.grid;
   const int64_t lo = Lc + ((Hc - Lc) * warp) / nwarps, hi = Lc + ((Hc - Lc) * (warp + 1)) / nwarps;
   const int stages = a.stages;
-  const uint64_t ring_bytes = static_cast<uint64_t>(nwarps) * stages * SB;
-  uint8_t* ring = smem + static_cast<uint64_t>(warp) * stages * SB;
+  // shared memory: ring [warps][stages] chunks | barriers | row slots | counters |
+  // x slices [warps][stages][MT] | per-warp scratch [warps][MT], or the x-slice cache
+  const uint64_t ring_bytes = static_cast<uint64_t>(nwarps) * stages * CB;
+  uint8_t* ring = smem + static_cast<uint64_t>(warp) * stages * CB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ring_bytes) + warp * stages;
-  uint8_t* tail = smem + ring_bytes + align16(static_cast<uint64_t>(nwarps) * stages * 8);
-  const uint32_t scratch = smem_u32(tail) + warp * MT * kScratchBytes;
-  float* slots = reinterpret_cast<float*>(tail + nwarps * MT * kScratchBytes);   // [nwarps][2][MT][32]
+  uint8_t* p8 = smem + ring_bytes + align16(static_cast<uint64_t>(nwarps) * stages * 8);
+  float* slots = reinterpret_cast<float*>(p8);                                   // [nwarps][2][MT][32]
   uint32_t* cnt = reinterpret_cast<uint32_t*>(slots + nwarps * 2 * MT * 32);     // [nwarps][2]
+  uint8_t* tail = reinterpret_cast<uint8_t*>(cnt) + align16(static_cast<uint64_t>(nwarps) * 8);
+  uint8_t* xsl = tail + static_cast<uint64_t>(warp) * stages * MT * kXSliceBytes;
+  const uint32_t tail2 = smem_u32(tail) + nwarps * stages * MT * kXSliceBytes;
+  const uint32_t scratch = tail2 + warp * MT * kScratchBytes;
+  const uint32_t xcache = tail2;
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur{}, pre{};                         // chunk being processed / next chunk to fetch
@@ -786,12 +893,36 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
-    // weights never change between launches: fetch the first chunks before waiting on the previous grid
+    // weights never change between launches: fetch the first chunks before
+    // waiting on the previous grid; their x slices follow after the wait
     Pos p = pre;
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_chunk<KIND, MT>(a, p, m, ring + s * SB, &bars[s]);
+      issue_chunk<KIND, MT>(a, p, static_cast<uint32_t>(m * kXSliceBytes), ring + s * CB, &bars[s]);
       p.next(a);
     }
+  }
+  if (XC && a.xslots > 0 && threadIdx.x == 32 * (nwarps - 1)) {
+    // which (item, tile column) slices the CTA's chunks touch; the cache is
+    // used when they fit and each is reused four times on average (below
+    // that, filling it costs the short launches more than it saves)
+    Pos p0{}, p1{};
+    p0.seek(a, Lc);
+    p1.seek(a, Hc - 1);
+    int ok = p1.it - p0.it < kXTabItems, total = 0;
+    for (int it = p0.it; ok && it <= p1.it; ++it) {
+      const GemvItemDev& I = a.items[it];
+      const int64_t ca = (Lc > I.cbase ? Lc : I.cbase) - I.cbase;
+      const int64_t ce = (Hc < I.cbase + I.nchunks ? Hc : I.cbase + I.nchunks) - I.cbase;
+      const bool whole = ce - ca >= I.TC;
+      const int ns = whole ? I.TC : static_cast<int>(ce - ca);
+      s_xtab[it - p0.it] = make_int4(total, whole ? 0 : static_cast<int>(ca % I.TC), ns, I.TC);
+      total += ns;
+      ok = total <= a.xslots;
+    }
+    s_xinfo[0] = ok && Hc - Lc >= 4 * static_cast<int64_t>(total);
+    s_xinfo[1] = p0.it;
+    s_xinfo[2] = total;
+    s_xinfo[3] = p1.it - p0.it + 1;
   }
   if (warp == 0 && lane < nwarps) s_wlo[lane] = static_cast<uint32_t>(((Hc - Lc) * lane) / nwarps);
   if (threadIdx.x == blockDim.x - 1) {
@@ -805,13 +936,44 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   __syncwarp();
   // the row counters are zero and the tables written before any warp can
   // count; done before the wait, so that no CTA-wide barrier follows it
+  // (except the one after the x-slice cache is filled)
   __syncthreads();
+  const bool xc = XC && a.xslots > 0 && s_xinfo[0] != 0;      // this CTA's x slices come from the cache
+  const uint32_t xbytes = xc ? 0u : static_cast<uint32_t>(m * kXSliceBytes);   // x bytes with each refill
   asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
   if (lane == 0) {
+    // the x slices of the chunks already in flight (unused when the cache serves them)
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_xslice<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
+      issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
       pre.next(a);
     }
+  }
+  if (xc) {
+    // fill the cache: warp w prepares slices w, w + nwarps, ...; each lane
+    // loads its 16 bytes of up to four slices before preparing any
+    const int nsl = s_xinfo[2], it0 = s_xinfo[1], nti = s_xinfo[3];
+    const int gp = lane & 7, tp = lane >> 3;
+    for (int s0 = warp; s0 < nsl; s0 += 4 * nwarps) {
+      uint4 xr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sl = s0 + u * nwarps;
+        if (sl < nsl) {
+          int k = 0;                                  // the touched item holding slot sl
+          while (k + 1 < nti && s_xtab[k + 1].x <= sl) ++k;
+          const int4 e = s_xtab[k];
+          int tc = e.y + (sl - e.x);
+          if (tc >= e.w) tc -= e.w;
+          xr[u] = ld_cg_u4(a.items[it0 + k].x + static_cast<int64_t>(tc) * kXSliceBytes + gp * 64 + tp * 16);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sl = s0 + u * nwarps;
+        if (sl < nsl) xslot_fill(xr[u], xcache + sl * kXSlotBytes, lane);
+      }
+    }
+    __syncthreads();
   }
 
   float yacc[MT][8];
@@ -841,19 +1003,37 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       seg_it = cur.it;
       seg_tr = cur.tr;
     }
-    const uint32_t st = smem_u32(ring + s * SB);
+    const uint32_t st = smem_u32(ring + s * CB);
+    const uint32_t xs = smem_u32(xsl + s * MT * kXSliceBytes);
     // 4-bit chunks: the lanes take their share of the stage into registers
     // and the stage is refilled before the arithmetic; Q8: after it
     Q4Lane<Q4 ? KIND : kQ4_1, MT> q4l;
-    if constexpr (Q4) q4_read<KIND, MT>(st, lane, m, q4l);
-    else q8_chunk<KIND, MT>(st, lane, m, yacc);
+    if constexpr (Q4) q4_read<KIND, MT>(st, xs, !xc, lane, m, q4l);
+    else q8_chunk<KIND, MT>(st, xs, lane, m, yacc);
     __syncwarp();
     if (lane == 0 && j + stages < n) {
-      issue_chunk<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
-      issue_xslice<KIND, MT>(a, pre, m, ring + s * SB, &bars[s]);
+      issue_chunk<KIND, MT>(a, pre, xbytes, ring + s * CB, &bars[s]);
+      if (!xc) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
       pre.next(a);
     }
-    if constexpr (Q4) q4_compute<KIND, MT>(q4l, scratch, lane, m, yacc);
+    if constexpr (Q4) {
+      if (XC && xc) {
+        const uint32_t sa = xcache + xslot_of(cur) * kXSlotBytes;
+        const uint32_t gr = sa + kXSlotG + (lane & 7) * 32;
+        const uint4 g0 = lds128(gr), g1 = lds128(gr + 16);
+        XGroup G[MT];
+        G[0].q0 = __uint_as_float(g0.x);
+        G[0].xq[0] = __uint_as_float(g0.y);
+        G[0].xq[1] = __uint_as_float(g0.z);
+        G[0].xq[2] = __uint_as_float(g0.w);
+        G[0].xq[3] = __uint_as_float(g1.x);
+        if (g1.y == 3u) q4_fixed<KIND, MT, 3>(q4l, sa, lane, m, G, yacc);        // (the slice's mode: uniform)
+        else if (g1.y == 4u) q4_fixed<KIND, MT, 4>(q4l, sa, lane, m, G, yacc);
+        else q4_float<KIND, MT>(q4l, sa, lane, m, yacc);
+      } else {
+        q4_compute<KIND, MT>(q4l, scratch, lane, m, yacc);
+      }
+    }
     cur.next(a);
     if (++s == stages) s = 0;
   }
@@ -904,11 +1084,14 @@ static int gemv_max_warps(int kind, int MT) {
 bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT) {
   const int CB = chunk_bytes_of(kind);
   if (CB == 0 || info.sms <= 0 || T <= 0 || MT < 1) return false;
-  const uint64_t SB = static_cast<uint64_t>(CB) + static_cast<uint64_t>(MT) * kXSliceBytes;
-  auto need = [&](int w, int st) {
-    return static_cast<uint64_t>(w) * st * SB + align16(static_cast<uint64_t>(w) * st * 8) +
-           static_cast<uint64_t>(w) * (MT * (kScratchBytes + kSlotBytes) + kCntBytes);
+  // ring, barriers, row slots, counters and the per-warp x slices; then the
+  // per-warp scratch, or (4-bit kinds, one token) the x-slice cache
+  auto base = [&](int w, int st) {
+    return static_cast<uint64_t>(w) * st * CB + align16(static_cast<uint64_t>(w) * st * 8) +
+           static_cast<uint64_t>(w) * MT * kSlotBytes + align16(static_cast<uint64_t>(w) * kCntBytes) +
+           static_cast<uint64_t>(w) * st * MT * kXSliceBytes;
   };
+  auto need = [&](int w, int st) { return base(w, st) + static_cast<uint64_t>(w) * MT * kScratchBytes; };
   // Eight warps per CTA, each streaming a longer run of chunks, measured best
   // on GB300 against 12 and 16.  4-bit chunks: the CTA stays within half an
   // SM's shared memory, so that the next launch in the stream (programmatic
@@ -957,6 +1140,14 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
   p->stages = stages;
   p->grid = static_cast<int>(grid);
   p->smem = need(warps, stages);
+  p->xslots = 0;
+  if ((kind == kQ4_1 || kind == kQ4_K) && MT == 1 && cap > base(warps, stages)) {
+    // the x-slice cache takes what the budget leaves: 17 slots in half an SM
+    const uint64_t room = (cap - base(warps, stages)) / kXSlotBytes;
+    p->xslots = static_cast<int>(room < static_cast<uint64_t>(kMaxXSlots) ? room : kMaxXSlots);
+    const uint64_t with_cache = base(warps, stages) + static_cast<uint64_t>(p->xslots) * kXSlotBytes;
+    if (with_cache > p->smem) p->smem = with_cache;
+  }
   return true;
 }
 
@@ -1030,6 +1221,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   fill_workspace(a, workspace);
   a.grid = p.grid;
   a.stages = p.stages;
+  a.xslots = p.xslots;
   a.out_f32 = out_f32;
   a.m = 1;
   a.x_stride = 0;
@@ -1086,6 +1278,7 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
   a.err = err;
   a.grid = p.grid;
   a.stages = p.stages;
+  a.xslots = p.xslots;
   a.out_f32 = out_f32;
   a.m = M;
   a.x_stride = item.TC * 256 * 2;                 // X rows: cols bf16 each

@@ -239,3 +239,38 @@ def test_gemm_64_tokens_with_outliers(q, N, K):
                                      np.random.default_rng(3).integers(0, N, 256)]))
     Y64, A = oracle.matmul(w, synth.Q4_1, N, K, X, rows=rows)
     assert_within(got[:, rows], Y64, A, True, f"gemm 64 tokens outliers {N}x{K}", bf16_weights=True)
+
+
+# ---------------------------------------------- x-slice cache coverage --
+
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K])
+@pytest.mark.parametrize("N,K", [(1024, 7168), (160, 1280), (4096, 7680), (96, 8192)])
+def test_cached_x_slices_partial_rows(q, kind, N, K):
+    """Shapes whose CTAs hold fewer chunks than a tile row (the touched tile
+    columns start mid-row and wrap) or exactly the cache's capacity, with
+    activations that make some x slices exact in 24-bit fixed point and
+    others not (outliers next to N(0, 1) columns, and one log-uniform slice)."""
+    f, w = synth.make(kind, N, K, synth.rng(51, kind, N))
+    x = synth.activations_outliers(synth.rng(51, 1, K), 1, K, frac=0.002)[0]
+    x[256:512] = synth.activations_log_uniform(synth.rng(51, 2), 1, 256)[0]
+    for out in ("f32", "bf16"):
+        check_gemv(q, kind, w, N, K, x, out, f"cache kind {kind} {N}x{K}")
+
+
+def test_cached_x_slices_many_items_per_cta(q):
+    """A batch of 40 small q4_1 matrices of mixed widths: some CTAs touch more
+    items than the cache's item table holds and prepare x per chunk, others
+    use the cache; every output matches the oracle."""
+    items, refs = [], []
+    g = np.random.default_rng(7)
+    for i in range(40):
+        N, K = 32 * int(g.integers(1, 4)), 256 * int(g.integers(1, 6))
+        f, w = synth.make(synth.Q4_1, N, K, synth.rng(52, 0, i))
+        x = (synth.activations_outliers if i % 3 == 0 else synth.activations)(synth.rng(52, 1, i), 1, K)[0]
+        y = torch.empty(N, dtype=torch.float32, device=DEV)
+        items.append((q.Weight(to_dev_bytes(w), synth.Q4_1, N, K), to_dev_bf16(x), y))
+        refs.append((w, x, N, K))
+    q.q4nx_gemv_batch(items, out_dtype="f32")
+    for (W, xt, y), (w, x, N, K) in zip(items, refs):
+        Y64, A = oracle.matmul(w, synth.Q4_1, N, K, x)
+        assert_within(out_values(y), Y64, A, False, f"batch item {N}x{K}")
