@@ -19,6 +19,14 @@ e2e        = the same metric through the public API with host buffers: per step
 roofline   = the dominant kernel (q4nx GEMV): algorithmic bytes per launch
              (chunks + x + y) / mean launch duration, against the measured HBM
              copy bandwidth.
+repeats    = the same K-step region timed again back to back (min / median / max).
+secondary  = every configuration's kernels timed on their own over rotated weight
+             copies (>= 512 MB, back to back): q4_1 1024x1024 GEMV and decode;
+             Q4_K 9728x2560 / 2560x9728 GEMV and repack; q4_1 12288x4096 /
+             4096x12288 at one token (fraction of the HBM copy peak) and at 64
+             tokens (TFLOP/s, fraction of the bytes-or-tensor roofline); the Q8
+             lm_head 151936x2560 in both layouts (GEMV, GEMV + top-1, 64-token
+             GEMM) and the argmax of 1 and 64 logit rows.
 cpu_baseline / --impl reference = the oracle (plain C, binary64, one core)
              on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
@@ -305,10 +313,25 @@ def run_gpu(args, rank: int, world: int):
     stream.synchronize()
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = ms / args.steps
     value = job_throughput(world, wtot, args.steps, ms / 1e3)
+
+    # the same K-step region timed again, for its spread (the line's value is the first timing)
+    rep_ms = [ms_per_step]
+    for _ in range(args.repeats):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        with torch.cuda.stream(stream):
+            a_.record(stream)
+            for _ in range(args.steps // per_graph):
+                graph_many.replay()
+            if graph_rem is not None:
+                graph_rem.replay()
+            b_.record(stream)
+        stream.synchronize()
+        rep_ms.append(max_over_ranks(a_.elapsed_time(b_), world, dev) / args.steps)
+    clk = clocks.stop()
 
     # other schedules of the same step, for context (not the headline)
     def time_graph(g, n):
@@ -325,7 +348,9 @@ def run_gpu(args, rank: int, world: int):
     alt = {}
     if not args.no_alt:
         g_layer = capture(lambda: [b() for b in per_layer])
-        alt["per_layer_4_launches_gbs"] = wtot / (time_graph(g_layer, 200) / 1e3) / 1e9
+        t_layer_ms = time_graph(g_layer, 200)
+        alt["per_layer_4_launches_gbs"] = wtot / (t_layer_ms / 1e3) / 1e9
+        alt["us_per_layer_dependent"] = t_layer_ms * 1e3 / synth.QWEN3_06B_LAYERS
         g_single = capture(lambda: [q.q4nx_gemv(weights[i], xs[i], out=ys[i], ws=ws) for i in range(len(mats))])
         alt["one_launch_per_matrix_gbs"] = wtot / (time_graph(g_single, 100) / 1e3) / 1e9
         del g_layer, g_single
@@ -356,6 +381,10 @@ def run_gpu(args, rank: int, world: int):
     t_e2e = max_over_ranks(t_e2e, world, dev)
     e2e_value = job_throughput(world, wtot, e2e_steps, t_e2e)
 
+    secondary = None
+    if rank == 0 and not args.no_secondary:
+        secondary = secondary_configs(q, Kit(torch, dev, stream))
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         b, t, m = cpu_oracle_sample(mats, _gen, args.cpu_seconds)
@@ -374,46 +403,55 @@ def run_gpu(args, rank: int, world: int):
                        "launch": "one q4nx_gemv_batch launch of all 196 matrices per step; CUDA graphs of "
                                  f"{per_graph} consecutive steps, replayed back to back",
                        "us_per_layer": ms_per_step * 1e3 / synth.QWEN3_06B_LAYERS,
+                       "us_per_layer_note": "all 28 layers' GEMVs in one launch (independent x per matrix); "
+                                            "the dependent schedule ({q,k,v} -> o -> {gate,up} -> down, each "
+                                            "phase one batched launch) is other_schedules.us_per_layer_dependent",
                        "other_schedules": alt,
                        "hbm_frac_of_nominal_8tbs": value / 8000.0},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                         "traffic_source": "stored ncu capture of this kernel (profiles/traffic.json, "
+                                           "dram read + write per launch); null when the kernel's sources "
+                                           "differ from the captured ones",
                          "bytes_per_launch": alg_bytes_step / launches_per_step,
                          "launch_us": launch_us},
+            "repeats": {"n": len(rep_ms), "ms_per_step_min": min(rep_ms),
+                        "ms_per_step_median": statistics.median(rep_ms), "ms_per_step_max": max(rep_ms),
+                        "note": "the K-step timed region, timed again back to back; value uses the first"},
+            "secondary": secondary,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * xtot,
                     "d2h_bytes_per_step": 2 * ytot},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
+            "clocks_window": "sampled over the timed region and its repeats",
         }
         print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------- suite --
+# ------------------------------------------------------------ timing kit --
 
-def run_suite(args):
-    """One JSON line per (workload, kernel): every kernel of the path timed on
-    the workload shapes, rotating through weight copies that together exceed
-    512 MB so that no launch finds its weights in L2."""
-    import torch
+class Kit:
+    """Back-to-back timing of launches: CUDA graphs over rotated input copies
+    (together at least 512 MB, so that no launch finds its weights in L2),
+    CUDA events on the launching stream."""
 
-    import dequant_gemv_gb300 as q
+    def __init__(self, torch, dev, stream):
+        self.torch, self.dev, self.stream = torch, dev, stream
+        self.hbm, _ = _peaks()
+        self.tc_peak = 1971.6
+        p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+        if os.path.exists(p):
+            with open(p) as f:
+                self.tc_peak = float(json.load(f).get("bf16_tflops", self.tc_peak))
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    hbm, _ = _peaks()
-    tc_peak = 1971.6
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            tc_peak = float(json.load(f).get("bf16_tflops", tc_peak))
-    stream = torch.cuda.Stream(dev)
-
+    @staticmethod
     def copies_for(nbytes):
         return max(2, min(1024, (512 << 20) // max(nbytes, 1) + 1))
 
-    def timeit(fns, iters):
-        """Time `iters` launches cycling over the callables in `fns` (one per copy), CUDA graph replay."""
+    def timeit(self, fns, iters):
+        """us per launch of `iters` launches cycling over the callables in `fns` (one per copy)."""
+        torch, stream = self.torch, self.stream
         with torch.cuda.stream(stream):
             for f in fns:
                 f()
@@ -432,16 +470,137 @@ def run_suite(args):
                 g.replay()
             b.record(stream)
         stream.synchronize()
-        return a.elapsed_time(b) * 1e3 / (reps * per_graph)      # us per launch
+        return a.elapsed_time(b) * 1e3 / (reps * per_graph)
+
+    def dev_bytes(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def dev_bf16(self, bits):
+        t = self.torch
+        return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(self.dev).view(t.bfloat16)
+
+    def hbm_frac(self, nbytes, us):
+        return nbytes / us / 1e3 / self.hbm
+
+    def roofline_us(self, nbytes, flops):
+        """The bytes-or-tensor roofline time of one launch (HBM copy peak, bf16 tensor burst peak)."""
+        return max(nbytes / (self.hbm * 1e3), flops / (self.tc_peak * 1e6))
+
+
+def secondary_configs(q, kit):
+    """The five configurations' kernels, each timed on its own (rotated weight
+    copies, back to back): one-token GEMVs with their fraction of the measured
+    HBM copy bandwidth; 64-token GEMMs with TFLOP/s and their fraction of the
+    bytes-or-tensor roofline; the decode, repack and top-1 kernels."""
+    import ctypes
+
+    torch = kit.torch
+    dev = kit.dev
+    out = {}
+
+    def weights(kind, N, K, wid, f=None):
+        if f is None:
+            f, w = synth.make(kind, N, K, synth.rng(wid, 0, 0))
+        else:
+            f.kind = kind
+            w = synth.pack(f)
+        base = kit.dev_bytes(w)
+        Ws = [q.Weight(base if r == 0 else base.clone(), kind, N, K) for r in range(kit.copies_for(w.size))]
+        return f, w.size, Ws
+
+    def gemv(Ws, N, K, nb, wid, out_f32):
+        x = kit.dev_bf16(synth.workload_activations(wid, 0, 1, K)[0])
+        y = torch.empty(N, dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
+        with torch.cuda.stream(kit.stream):
+            ws = torch.zeros(int(q.lib.q4nx_gemv_workspace(ctypes.byref(Ws[0].c()))), dtype=torch.uint8, device=dev)
+        od = "f32" if out_f32 else "bf16"
+        us = kit.timeit([lambda W=W: q.q4nx_gemv(W, x, out=y, out_dtype=od, ws=ws) for W in Ws], 400)
+        alg = nb + 2 * K + (4 if out_f32 else 2) * N
+        return {"gemv_us": round(us, 3), "gemv_frac": round(kit.hbm_frac(alg, us), 4), "_x": x, "_ws": ws}
+
+    def gemm(Ws, N, K, nb, wid, out_f32, M=64):
+        X = kit.dev_bf16(synth.workload_activations(wid, 0, M, K))
+        Y = torch.empty((M, N), dtype=torch.float32 if out_f32 else torch.bfloat16, device=dev)
+        with torch.cuda.stream(kit.stream):
+            ws = torch.zeros(int(q.lib.q4nx_gemm_workspace(ctypes.byref(Ws[0].c()), M)), dtype=torch.uint8, device=dev)
+        od = "f32" if out_f32 else "bf16"
+        us = kit.timeit([lambda W=W: q.q4nx_gemm_m64(W, X, out=Y, out_dtype=od, ws=ws) for W in Ws], 200)
+        flops = 2.0 * M * N * K
+        alg = nb + 2 * M * K + (4 if out_f32 else 2) * M * N
+        t_roof = kit.roofline_us(alg, flops)
+        return {"gemm_m64_us": round(us, 3), "gemm_m64_tflops": round(flops / us / 1e6, 1),
+                "gemm_m64_frac": round(t_roof / us, 4),
+                "gemm_m64_bound": "hbm" if alg / (kit.hbm * 1e3) >= flops / (kit.tc_peak * 1e6) else "tensor"}
+
+    def clean(d):
+        return {k: v for k, v in d.items() if not k.startswith("_")}
+
+    # 1: q4_1 1024x1024, decode + GEMV
+    f, nb, Ws = weights(synth.Q4_1, 1024, 1024, 1)
+    d = gemv(Ws, 1024, 1024, nb, 1, False)
+    outs = [torch.empty((1024, 1024), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    us = kit.timeit([lambda W=W, o=outs[i % 2]: q.q4nx_decode(W, out=o) for i, W in enumerate(Ws)], 200)
+    d.update({"decode_us": round(us, 3), "decode_frac": round(kit.hbm_frac(nb + 2 * 1024 * 1024, us), 4)})
+    out["q4_1_1024x1024"] = clean(d)
+    del Ws, outs
+    # 3: Q4_K GEMV and the repack, both shapes
+    for N, K in ((9728, 2560), (2560, 9728)):
+        f, nb, Ws = weights(synth.Q4_K, N, K, 3)
+        d = gemv(Ws, N, K, nb, 3, False)
+        rep = torch.empty((N // 32) * (K // 256) * 5120, dtype=torch.uint8, device=dev)
+        us = kit.timeit([lambda W=W: q.q4nx_repack_q4k(W.chunks, N, K, out=rep) for W in Ws], 200)
+        d.update({"repack_us": round(us, 3), "repack_frac": round(kit.hbm_frac(nb + rep.numel(), us), 4)})
+        out[f"q4k_{N}x{K}"] = clean(d)
+        del Ws, rep
+    # 4: the 64-token prefill block's matrices (and the same matrices at one token)
+    for N, K in ((12288, 4096), (4096, 12288)):
+        f, nb, Ws = weights(synth.Q4_1, N, K, 4)
+        d = gemv(Ws, N, K, nb, 4, False)
+        d.update(gemm(Ws, N, K, nb, 4, False))
+        out[f"q4_1_{N}x{K}"] = clean(d)
+        del Ws
+    # 5: the Q8 lm_head in both code layouts: logits + top-1, one token and 64
+    fq = None
+    for kind, name in ((synth.Q8_KR, "kr"), (synth.Q8_BLK, "blk")):
+        fq, nb, Ws = weights(kind, 151936, 2560, 5, fq)
+        d = gemv(Ws, 151936, 2560, nb, 5, True)
+        idx1 = torch.empty(1, dtype=torch.int32, device=dev)
+        us = kit.timeit([lambda W=W: q.q4nx_gemv_top1(W, d["_x"], out=idx1, ws=d["_ws"]) for W in Ws], 200)
+        d.update({"gemv_top1_us": round(us, 3), "gemv_top1_frac": round(kit.hbm_frac(nb + 2 * 2560 + 4, us), 4)})
+        d.update(gemm(Ws, 151936, 2560, nb, 5, True))
+        out[f"q8_{name}_151936x2560"] = clean(d)
+        del Ws, d
+    for M in (1, 64):
+        L = torch.randn((M, 151936), generator=torch.Generator(device="cpu").manual_seed(M),
+                        dtype=torch.float32).to(dev)
+        idx = torch.empty(M, dtype=torch.int32, device=dev)
+        Ls = [L] + [L.clone() for _ in range(max(1, min(1024, (512 << 20) // L.numel() // 4)))]
+        us = kit.timeit([lambda Lm=Lm: q.q4nx_argmax(Lm, out=idx) for Lm in Ls], 400)
+        out[f"argmax_{M}x151936"] = {"us": round(us, 3), "frac": round(kit.hbm_frac(4 * M * 151936, us), 4)}
+        del Ls, L
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------- suite --
+
+def run_suite(args):
+    """One JSON line per (workload, kernel): every kernel of the path timed on
+    the workload shapes, rotating through weight copies that together exceed
+    512 MB so that no launch finds its weights in L2."""
+    import torch
+
+    import dequant_gemv_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    kit = Kit(torch, dev, stream)
+    hbm, tc_peak = kit.hbm, kit.tc_peak
+    copies_for, timeit, dev_bytes, dev_bf16 = kit.copies_for, kit.timeit, kit.dev_bytes, kit.dev_bf16
 
     def emit(d):
         print(json.dumps(d), flush=True)
-
-    def dev_bytes(a):
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    def dev_bf16(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
     cases = [
         (1, "q4_1 1024x1024", synth.Q4_1, 1024, 1024),
@@ -616,6 +775,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-alt", action="store_true", help="skip timing the other launch schedules")
+    ap.add_argument("--no-secondary", action="store_true", help="skip timing the other configurations' kernels")
+    ap.add_argument("--repeats", type=int, default=6, help="extra timings of the K-step region (spread)")
     ap.add_argument("--suite", action="store_true", help="time every kernel on every workload shape (JSON lines)")
     ap.add_argument("--only", default="", help="suite: comma list of gemv,top1,decode,repack,pack,gemm_small_m,gemm_m64,argmax,block")
     ap.add_argument("--case", default="", help="suite: substring of the workload name")

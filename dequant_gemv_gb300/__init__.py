@@ -83,6 +83,7 @@ def _load():
         "q4nx_check": ([P, P], I),
         "q4nx_gemv_noalloc": ([W, P, P, I, P], I),
         "q4nx_noalloc_scratch_bytes": ([], U64),
+        "q4nx_check_noalloc": ([P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -94,7 +95,7 @@ def _load():
 lib = _load()
 EXPORTS = ("q4nx_chunk_bytes", "q4nx_status_str", "q4nx_abi_version", "q4nx_decode", "q4nx_gemv",
            "q4nx_gemv_workspace", "q4nx_gemv_top1", "q4nx_gemv_top1_key", "q4nx_gemv_batch", "q4nx_gemv_batch_workspace", "q4nx_gemm_m64", "q4nx_gemm_workspace", "q4nx_repack_q4k", "q4nx_pack_q4_1", "q4nx_argmax",
-           "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes")
+           "q4nx_check", "q4nx_gemv_noalloc", "q4nx_noalloc_scratch_bytes", "q4nx_check_noalloc")
 
 
 def q4nx_chunk_bytes(kind: int) -> int:
@@ -337,6 +338,14 @@ def q4nx_gemv_noalloc(w: Weight, x: torch.Tensor, out: torch.Tensor | None = Non
         _check(lib.q4nx_gemv_noalloc(ctypes.byref(cw), x.data_ptr(), out.data_ptr(), code, _stream(w.device)),
                "q4nx_gemv_noalloc")
     return out
+
+
+def q4nx_check_noalloc(device=None) -> None:
+    """Raise Q4NXError if a bounded in-kernel wait of an earlier q4nx_gemv_noalloc
+    call on this device gave up (synchronises the current stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(lib.q4nx_check_noalloc(_stream(dev)), "q4nx_check_noalloc")
 
 
 def q4nx_gemm_m64(w: Weight, X: torch.Tensor, out: torch.Tensor | None = None, out_dtype="bf16",

@@ -9,6 +9,7 @@
 #include <cstring>
 
 #include "../../include/q4nx.h"
+#include "q4nx_checks.h"
 #include "q4nx_device.cuh"
 #include "q4nx_kernels.h"
 
@@ -83,9 +84,7 @@ cudaError_t set_max_dynamic_smem(const void* func, int slot) {
 
 using namespace q4nx;
 
-namespace {
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+namespace q4nx {
 
 int check_grid(int64_t rows, int64_t cols) {
   if (rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 256 != 0) return Q4NX_E_SHAPE;
@@ -104,6 +103,10 @@ int check_weight(const q4nx_weight* w) {
   if (!aligned16(w->chunks_dev)) return Q4NX_E_ALIGN;
   return Q4NX_OK;
 }
+
+}  // namespace q4nx
+
+namespace {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? Q4NX_OK : Q4NX_E_CUDA; }
 

@@ -6,12 +6,14 @@
 // the caller; this entry point instead uses kNoAllocScratchBytes of statically
 // allocated device memory that every GPU loading the library holds until the
 // process exits.  Host code never dereferences the array's name: the device
-// address is looked up once per device with cudaGetSymbolAddress and passed
-// to the kernel like any other pointer.
-#include <atomic>
+// address of the current device's copy is looked up with cudaGetSymbolAddress
+// on every call (a host-side lookup; it stays right after a device reset, which
+// can load the library's device code at another address) and passed to the
+// kernel like any other pointer.
 #include <cstdint>
 
 #include "../../include/q4nx.h"
+#include "q4nx_checks.h"
 #include "q4nx_device.cuh"
 #include "q4nx_kernels.h"
 
@@ -19,25 +21,14 @@ namespace q4nx {
 namespace {
 
 constexpr uint64_t kNoAllocScratchBytes = uint64_t(1) << 20;   // 1 MiB
-constexpr int kMaxDevicesNoAlloc = 64;
 
 static __device__ __align__(256) uint8_t g_gemv_scratch[kNoAllocScratchBytes];
 
-std::atomic<void*> g_scratch_addr[kMaxDevicesNoAlloc];
-
-// Device address of this device's copy of the scratch array; looked up on the
-// first call made with that device current.
+// Device address of the current device's copy of the scratch array.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevicesNoAlloc) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    e = cudaGetSymbolAddress(&p, g_gemv_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
-  }
   *out = p;
   return cudaSuccess;
 }
@@ -52,17 +43,13 @@ extern "C" {
 uint64_t q4nx_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype, void* stream) {
-  if (w == nullptr || w->chunks_dev == nullptr || x_dev == nullptr || y_dev == nullptr) return Q4NX_E_NULL;
-  const uint64_t cb = q4nx_chunk_bytes(w->kind);
-  if (cb == 0 || w->reserved != 0) return Q4NX_E_KIND;
-  if (w->rows <= 0 || w->cols <= 0 || w->rows % 32 != 0 || w->cols % 256 != 0) return Q4NX_E_SHAPE;
-  const int64_t TR = w->rows / 32, TC = w->cols / 256;
-  if (TR > (int64_t(1) << 31) / TC) return Q4NX_E_SHAPE;
-  if (w->bytes < static_cast<uint64_t>(TR) * static_cast<uint64_t>(TC) * cb) return Q4NX_E_SHORT;
-  if ((reinterpret_cast<uintptr_t>(w->chunks_dev) | reinterpret_cast<uintptr_t>(x_dev) |
-       reinterpret_cast<uintptr_t>(y_dev)) & 15u)
-    return Q4NX_E_ALIGN;
+  // the same checks, in the same order, as q4nx_gemv
+  int st = check_weight(w);
+  if (st) return st;
+  if (x_dev == nullptr || y_dev == nullptr) return Q4NX_E_NULL;
   if (out_dtype != Q4NX_OUT_BF16 && out_dtype != Q4NX_OUT_F32) return Q4NX_E_DTYPE;
+  if (!aligned16(x_dev) || !aligned16(y_dev)) return Q4NX_E_ALIGN;
+  const int64_t TR = w->rows / 32, TC = w->cols / 256;
   const uint64_t need = gemv_workspace_bytes(TR, TR * TC);
   if (need > kNoAllocScratchBytes) return Q4NX_E_WORKSPACE;          // cannot happen: the need is a constant
   void* scratch = nullptr;
@@ -84,6 +71,21 @@ int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int 
                  cudaSuccess
              ? Q4NX_OK
              : Q4NX_E_CUDA;
+}
+
+int q4nx_check_noalloc(void* stream) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return Q4NX_E_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t err = 0;
+  if (cudaMemcpyAsync(&err, scratch, sizeof err, cudaMemcpyDeviceToHost, s) != cudaSuccess) return Q4NX_E_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return Q4NX_E_CUDA;
+  if (err == 0) return Q4NX_OK;
+  // a wait gave up: clear the whole array (a call that gave up may have left
+  // posted sums in it; the next call clears what it uses anyway)
+  if (cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, s) != cudaSuccess) return Q4NX_E_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return Q4NX_E_CUDA;
+  return Q4NX_E_DEVICE_TIMEOUT;
 }
 
 }  // extern "C"

@@ -221,21 +221,32 @@ int q4nx_argmax(const float* logits_dev, int M, int64_t V, int32_t* idx_dev, voi
  * example a real-time decode loop, or a plug-in inside a framework that owns
  * every device allocation and hands out only inputs and outputs).  The pages
  * have no counterpart of this entry point; it is q4nx_gemv with its scratch
- * memory (error word, posted partial sums) taken from a 1 MiB
- * array compiled into the library, which every GPU that loads the library
- * keeps until the process exits.
- * The caller passes inputs and outputs only, exactly as for q4nx_gemv.
- * The first call on each device looks up that device's copy of the array
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Every call clears the scratch it uses, so a call never depends on what an
- * earlier call left behind; but all calls on a device share the one array, so
- * calls that can overlap on the GPU (different streams, or concurrent graph
- * branches) race and must be serialised by the caller.
- * The scratch a call needs does not grow with the weight, so every weight that
- * q4nx_gemv accepts fits q4nx_noalloc_scratch_bytes(); the statuses are those
- * of q4nx_gemv.  Calls no cudaMalloc or cudaFree. */
+ * memory (error word, posted partial sums) taken from a 1 MiB array compiled
+ * into the library, which every GPU that loads the library keeps until the
+ * process exits.
+ * The caller passes inputs and outputs only, exactly as for q4nx_gemv; the
+ * arguments are checked as q4nx_gemv checks them (same statuses, same order;
+ * there is no workspace to check).  Every call looks up the current device's
+ * copy of the array (cudaGetSymbolAddress, a host-side lookup); the first call
+ * on a device also loads the library's device code there, so make it before
+ * any stream capture.  Every call clears the scratch it uses before its
+ * launch, so a call never depends on what an earlier call left behind; but all
+ * calls on a device share the one array, so calls that can overlap on the GPU
+ * (different streams, or concurrent graph branches) race and must be
+ * serialised by the caller.  The scratch a call needs does not grow with the
+ * weight, so every weight that q4nx_gemv accepts fits
+ * q4nx_noalloc_scratch_bytes().  A bounded in-kernel wait that gives up
+ * (see q4nx_gemv) is reported by q4nx_check_noalloc, not by the call.  Calls
+ * no cudaMalloc or cudaFree. */
 int q4nx_gemv_noalloc(const q4nx_weight* w, const void* x_dev, void* y_dev, int out_dtype, void* stream);
 uint64_t q4nx_noalloc_scratch_bytes(void);
+
+/* The error word of q4nx_gemv_noalloc's built-in scratch on the current
+ * device: read it after the calls to check (synchronises `stream`) and before
+ * the next call, which clears it.  Q4NX_OK, or Q4NX_E_DEVICE_TIMEOUT if a
+ * bounded wait of an earlier call gave up (that call's outputs are invalid);
+ * the array is then cleared.  Q4NX_E_CUDA if the lookup or the copy fails. */
+int q4nx_check_noalloc(void* stream);
 
 /* Read and clear the error word of a workspace (synchronises `stream`).
  * Returns Q4NX_OK, or Q4NX_E_DEVICE_TIMEOUT if a bounded in-kernel wait of a

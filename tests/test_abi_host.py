@@ -151,6 +151,36 @@ def test_validation_statuses(q):
     assert L.q4nx_check(None, None) == 1
 
 
+def test_noalloc_statuses_equal_gemv_statuses(q):
+    """q4nx_gemv_noalloc checks its arguments as q4nx_gemv does (the same shared
+    checks, in the same order): every bad argument set gives both entry points
+    the same status, before any CUDA call."""
+    L = q.lib
+    by = ctypes.byref
+    P = 0x10000
+    need = L.q4nx_gemv_workspace(by(_w(q, ptr=P)))
+    cases = [
+        (None, P, P, 0),                                        # NULL weight
+        (_w(q, ptr=None), P, P, 0),                             # NULL chunks
+        (_w(q, ptr=P, kind=7), P, P, 0),                        # unknown kind
+        (_w(q, ptr=P, kind=2, nbytes=4735), P, P, 0),           # short Q4_K
+        (_w(q, ptr=P, reserved=3), P, P, 0),                    # reserved field
+        (_w(q, ptr=P, rows=33), P, P, 0),                       # shape
+        (_w(q, ptr=P, cols=512), P, P, 0),                      # buffer too short for 32x512
+        (_w(q, ptr=P + 8), P, P, 0),                            # misaligned chunks
+        (_w(q, ptr=P), None, P, 0),                             # NULL x
+        (_w(q, ptr=P), P, None, 0),                             # NULL y
+        (_w(q, ptr=P), P, P, 5),                                # unknown dtype
+        (_w(q, ptr=P), P + 4, P, 0),                            # misaligned x
+        (_w(q, ptr=P), P, P + 2, 1),                            # misaligned y
+    ]
+    for w, x, y, od in cases:
+        wp = None if w is None else by(w)
+        a = L.q4nx_gemv(wp, x, y, od, P, need, None)
+        b = L.q4nx_gemv_noalloc(wp, x, y, od, None)
+        assert a == b != 0, (w, x, y, od, a, b)
+
+
 def test_weight_tile_rows_is_pointer_arithmetic(q):
     import torch
 

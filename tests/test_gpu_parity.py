@@ -374,21 +374,59 @@ def test_argmax_signed_zeros_and_infs(q):
     assert np.array_equal(got, oracle.argmax(L))
 
 
+def _ambiguous_and_check(idx_gpu, logits, w, kind, N, K, X, bar_rel, what):
+    """Reading o12: per row, the top-1 of the GPU logits must equal the top-1 of
+    the binary64 oracle logits wherever the oracle's top-2 gap exceeds twice the
+    bar.  Rows below that gap are ambiguous (several answers are within the
+    bar): there the GPU's choice must be a row whose oracle logit lies within
+    twice the bar of the oracle's maximum, and it must still equal the oracle's
+    top-1 wherever the gap exceeds twice the GPU's own largest observed error on
+    the row's candidates (|y - y64| <= e everywhere and a gap > 2e fix the
+    answer).  The candidates are the row's 64 largest GPU logits.  Returns the
+    number of ambiguous rows."""
+    ambiguous = 0
+    for m in range(logits.shape[0]):
+        cand = np.argsort(-logits[m])[:64]
+        Y64, A = oracle.matmul(w, kind, N, K, X[m], rows=cand)
+        order = np.argsort(-Y64)
+        best, second = order[0], order[1]
+        gap = Y64[best] - Y64[second]
+        bar = bar_rel * max(A[best], A[second])
+        if gap > 2 * bar:
+            assert idx_gpu[m] == cand[best], f"{what}: row {m} top-1 {idx_gpu[m]} != oracle {cand[best]}"
+            continue
+        ambiguous += 1
+        chosen = np.nonzero(cand == idx_gpu[m])[0]
+        assert chosen.size == 1, f"{what}: row {m} top-1 {idx_gpu[m]} not among the 64 largest logits"
+        assert Y64[best] - Y64[chosen[0]] <= 2 * bar, f"{what}: row {m} chose a row outside the bar"
+        e_obs = float(np.max(np.abs(logits[m][cand].astype(np.float64) - Y64)))
+        if gap > 2 * e_obs:
+            assert idx_gpu[m] == cand[best], f"{what}: row {m}: gap {gap} > 2 x observed error {e_obs}"
+    return ambiguous
+
+
 @pytest.mark.parametrize("kind", [synth.Q8_KR, synth.Q8_BLK])
 def test_lm_head_top1(q, kind):
+    """lm_head logits then argmax, one token (GEMV) and 64 tokens (tensor-core
+    GEMM): q4nx_argmax equals the oracle's scan of the same GPU logits bit for
+    bit, and the end-to-end top-1 equals the binary64 oracle's on every
+    unambiguous row (see _ambiguous_and_check).  At these seeds the rows'
+    top-2 gaps are often inside twice the bar (the one-token row: 0.63 against
+    1.13), so the ambiguous count is printed, not assumed to be 0."""
     N, K = 151936, 2560
     f, w = synth.make(kind, N, K, synth.rng(5, 0, 0))
     W = q.Weight(to_dev_bytes(w), kind, N, K)
     x = synth.workload_activations(5, 0, 1, K)[0]
     logits = q.q4nx_gemv(W, to_dev_bf16(x), out_dtype="f32")
-    idx = int(q.q4nx_argmax(logits).cpu().numpy()[0])
-    lg = logits.cpu().numpy()
-    assert idx == int(oracle.argmax(lg))
-    # fp64 top-1 where unambiguous: the candidates are the top few GPU logits
-    cand = np.argsort(-lg)[:64]
-    Y64, A = oracle.matmul(w, kind, N, K, x, rows=cand)
-    order = np.argsort(-Y64)
-    best, second = order[0], order[1]
-    gap = Y64[best] - Y64[second]
-    if gap > 2 * REL * max(A[best], A[second]):
-        assert idx == cand[best]
+    idx = q.q4nx_argmax(logits.view(1, N)).cpu().numpy()
+    lg = logits.cpu().numpy().reshape(1, N)
+    assert np.array_equal(idx, oracle.argmax(lg))
+    amb1 = _ambiguous_and_check(idx, lg, w, kind, N, K, x.reshape(1, K), REL, f"kind {kind} M=1")
+    X = synth.workload_activations(5, 0, 64, K)
+    L64 = q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype="f32")
+    idx64 = q.q4nx_argmax(L64).cpu().numpy()
+    lg64 = L64.cpu().numpy()
+    assert np.array_equal(idx64, oracle.argmax(lg64))
+    # the tensor-core logits multiply bf16 weights: reading o21's bar
+    amb64 = _ambiguous_and_check(idx64, lg64, w, kind, N, K, X, REL + BF16_WEIGHTS, f"kind {kind} M=64")
+    print(f"lm_head top-1 kind {kind}: ambiguous rows {amb1} of 1 (GEMV), {amb64} of 64 (GEMM)")
