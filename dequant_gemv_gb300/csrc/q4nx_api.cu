@@ -7,6 +7,9 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/q4nx.h"
 #include "q4nx_checks.h"
@@ -20,8 +23,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_smem[kMaxDevices];
 std::atomic<int> g_smem_pair[kMaxDevices];
-// one flag per (device, kernel slot) that the max dynamic smem attribute was set
-std::atomic<uint32_t> g_attr_set[kMaxDevices];
+// the (device, kernel) pairs whose dynamic shared-memory limit has been raised
+std::mutex g_attr_mu;
+std::set<std::pair<int, const void*>> g_attr_set;
 }  // namespace
 
 cudaError_t device_info(DeviceInfo* out) {
@@ -56,15 +60,16 @@ cudaError_t device_info(DeviceInfo* out) {
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device maximum (less the
-// kernel's static shared memory), once per (device, slot).  Slots 0..31 are
-// free for the kernels to use.
-cudaError_t set_max_dynamic_smem(const void* func, int slot) {
+// kernel's static shared memory), once per (device, kernel).
+cudaError_t set_max_dynamic_smem(const void* func) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot > 31) return cudaErrorInvalidValue;
-  const uint32_t bit = 1u << slot;
-  if (g_attr_set[dev].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  if (dev < 0 || dev >= kMaxDevices || func == nullptr) return cudaErrorInvalidValue;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (g_attr_set.count({dev, func})) return cudaSuccess;
+  }
   DeviceInfo info;
   e = device_info(&info);
   if (e != cudaSuccess) return e;
@@ -76,7 +81,8 @@ cudaError_t set_max_dynamic_smem(const void* func, int slot) {
   if (dyn <= 0) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
-  g_attr_set[dev].fetch_or(bit, std::memory_order_acq_rel);
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  g_attr_set.insert({dev, func});
   return cudaSuccess;
 }
 

@@ -893,7 +893,7 @@ cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void
   if (grid > 1024) grid = 1024;
   if (grid < 1) grid = 1;
   a.grid = static_cast<int>(grid);
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm::gemm_kernel<KIND>), 16 + KIND);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm::gemm_kernel<KIND>));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid);

@@ -33,51 +33,9 @@
 //    first chunk, which reads the others' sums posted as (value, ready flag)
 //    words.  Partials are added in a fixed order, so results do not depend on
 //    timing, and the workspace is left zero-filled.
-#include "q4nx_device.cuh"
-#include "q4nx_kernels.h"
+#include "q4nx_gemv_common.cuh"
 
 namespace q4nx {
-
-constexpr int kXSliceBytes = 512;            // bf16 x of one tile column, per token
-constexpr int kScratchBytes = 1024;          // per warp and token: x digit planes (or the raw x slice) of one chunk
-constexpr int kSlotBytes = 2 * 32 * 4;       // per warp and token: sums of its first and last tile row
-constexpr int kCntBytes = 8;                 // per warp: arrival counters of its first and last tile row
-constexpr int kMaxBatch = kMaxGemvItems;
-
-struct GemvItemDev {
-  const uint8_t* chunks;
-  const uint8_t* x;        // bf16 [K] (token m at x + m * x_stride)
-  void* y;                 // [N] (token m at y + m * y_stride elements)
-  int64_t cbase;           // first chunk of this item in the batch index space
-  int64_t nchunks;         // TR * TC
-  int32_t TC;
-};
-
-// Kernel parameters; MAXB batch slots (instantiated for 1, 8 and 256 items so
-// that small launches do not carry a 12 KB parameter block).
-template <int MAXB>
-struct GemvArgsT {
-  GemvItemDev items[MAXB];
-  int nitems;
-  int grid;                // CTAs; CTA b owns chunks [T b / grid, T (b+1) / grid)
-  int stages;
-  int xslots;              // 4-bit kinds, one token: x-slice cache slots in shared memory (0: none)
-  int out_f32;
-  int m;                   // tokens (1 unless one item against several tokens)
-  int64_t x_stride;        // bytes between tokens' x
-  int64_t y_stride;        // elements between tokens' y
-  int64_t T;               // chunks in the batch
-  uint32_t* err;
-  uint64_t* posted;        // [grid][MT][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
-  // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
-  // row) key; the last CTA to finish writes the row index and/or the key
-  int top1;                // 0: store y
-  uint32_t top1_row_base;  // added to the rows in the keys (a shard's first row)
-  int32_t* top1_idx;       // null, or where the row goes
-  int64_t* top1_key_out;   // null, or where the key goes (top bit flipped: signed order = key order)
-  uint64_t* top1_key;      // workspace word, zero between launches
-  uint32_t* top1_done;     // workspace word, zero between launches
-};
 
 // This CTA's largest top-1 key so far (top-1 mode).
 __shared__ unsigned long long s_top1_key;
@@ -101,10 +59,6 @@ __shared__ long long s_clast;
 // needs the binary32 path; then per group 32 B: q0, xq0..xq3 and the slice's
 // mode (3 or 4 digit planes, 5 for binary32).  Slots of one item are its
 // touched tile columns in order, starting from column tc0 and wrapping.
-constexpr int kXSlotBytes = 1280;
-constexpr int kXSlotG = 1024;              // per-group records within a slot
-constexpr int kXTabItems = 16;
-constexpr int kMaxXSlots = 32;
 __shared__ int4 s_xtab[kXTabItems];        // per touched item: {first slot, tc0, slots, TC}
 __shared__ int s_xinfo[4];                 // cache used (0/1), first touched item, slots in use, items touched
 
@@ -129,9 +83,6 @@ __device__ __forceinline__ float transpose_reduce8(float v[8], int lane, int m2,
   float keep = b0 ? v[1] : v[0];
   return keep + __shfl_xor_sync(0xffffffffu, send, m0);
 }
-
-// CTA that holds chunk c: the largest b with floor(T*b/G) <= c
-__device__ __forceinline__ int64_t cta_of(int64_t c, int64_t T, int64_t G) { return ((c + 1) * G - 1) / T; }
 
 // Row n's final value (called by all 32 lanes of a warp together, one row
 // each): store it, or in top-1 mode fold it into the CTA's largest key.
@@ -163,8 +114,6 @@ __device__ __forceinline__ void store_y(const GemvArgs& a, void* y, int64_t n, f
 // the finisher reads the posted words (waiting, bounded, for any not yet
 // ready), adds them in CTA order after its own sum, stores y and clears the
 // words it used.
-constexpr uint64_t kPosted = 1ull << 32;
-
 template <int MT, class GemvArgs>
 __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t Lc, int it, int64_t tr, int64_t r0,
                                            int64_t r1, const float (&val)[MT], int lane) {
@@ -268,18 +217,6 @@ __device__ __noinline__ void cross_cta_row(const GemvArgs& a, int64_t b, int64_t
 // (a range of magnitudes beyond 2^14, values below 2^-105, Inf or NaN) take
 // the binary32 path instead for the whole chunk: w = fl(c s + z), then an fma
 // per weight.
-__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-  int d;
-  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-
 // A q4 chunk's share of one lane, read out of the ring stage at once so that
 // the stage can be refilled before the arithmetic starts.  Prep lane
 // (gp = lane & 7, tp = lane >> 3) reads the 8 columns gp*32 + 8tp .. +7 of
@@ -325,98 +262,6 @@ __device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, 
   } else {                                         // exact products: 8 x 6 significant bits
     s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * static_cast<float>(L.f1[i] & 0xFFFFu);
     z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
-  }
-}
-
-// Per token, for the lane's group g = lane & 7 (prep and decode lanes of a
-// group share the low three lane bits): the weight of the lowest digit plane
-// and the digit sums times the plane weights.
-struct XGroup {
-  float q0;                        // 2^(E - 124 - 8 NP); plane p weighs q0 256^p
-  float xq[4];                     // X_p q0 256^p
-};
-
-// How many digit planes one token's x slice needs for this lane's group (all
-// four prep lanes of the group get the same answer): 3 when every value is a
-// multiple of 2^(E-148) below 2^(E-126) (E the biased exponent of the group's
-// largest |x|: nonzero values within 2^14 of the largest, 22 <= E <= 254), 4
-// when within 2^22 (30 <= E <= 254, step 2^(E-156)), else 5 (none does: the
-// binary32 path).  An all-zero group needs 3.
-__device__ __forceinline__ int q4_x_need(const uint4 xr, int& E) {
-  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-  const uint32_t m2 = __vmaxu2(__vmaxu2(xw[0] & 0x7FFF7FFFu, xw[1] & 0x7FFF7FFFu),
-                               __vmaxu2(xw[2] & 0x7FFF7FFFu, xw[3] & 0x7FFF7FFFu));
-  uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
-  // smallest nonzero |x| as (binary32 bits << 1) - 1: the sign drops out and
-  // +-0 becomes 0xFFFFFFFF, above every other key
-  uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    mn = min(mn, (xw[j] << 17) - 1u);
-    mn = min(mn, ((xw[j] & 0xFFFF0000u) << 1) - 1u);
-  }
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 8));
-  mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 16));
-  E = static_cast<int>(mx >> 7);
-  const int emin = static_cast<int>((mn + 1u) >> 24);    // exponent field of the smallest nonzero |x|
-  if (mx == 0 || (E >= 22 && E <= 254 && emin >= E - 14)) return 3;
-  if (E >= 30 && E <= 254 && emin >= E - 22) return 4;
-  return 5;
-}
-
-// One token's x slice (this prep lane's 8 columns) -> NP digit planes in
-// `scratch`: region A [t][g] 16 B (p0 even, p0 odd, p1 even, p1 odd) and
-// region B at +512 [t][g] 16 B (p2 even, p2 odd, p3 even, p3 odd); and the
-// group's plane weight and digit sums.  v_k = x_k 2^(124 + 8 NP - E), |v_k| <
-// 2^(8 NP - 2), exact by q4_x_need; v_k + 0x80..80 has the bytes d_p + 128.
-template <int NP>
-__device__ __forceinline__ void q4_x_planes(const uint4 xr, int E, uint32_t scratch, int lane, XGroup& G) {
-  const int gp = lane & 7, tp = lane >> 3;
-  E = min(max(E, 8 * NP - 2), 254);                              // (an all-zero group: any step)
-  const float sc = __int_as_float((251 + 8 * NP - E) << 23);     // 2^(124 + 8 NP - E)
-  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
-  uint32_t v[8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float f0 = __uint_as_float(xw[j] << 16), f1 = __uint_as_float(xw[j] & 0xFFFF0000u);
-    if constexpr (NP == 3) {                                     // |v| < 2^22: round by the 1.5 * 2^23 magic number
-      v[2 * j] = __float_as_uint(fmaf(f0, sc, 12582912.0f)) - 0x4ABF7F80u;
-      v[2 * j + 1] = __float_as_uint(fmaf(f1, sc, 12582912.0f)) - 0x4ABF7F80u;
-    } else {                                                     // |v| < 2^30: an integer conversion
-      v[2 * j] = static_cast<uint32_t>(__float2int_rn(f0 * sc)) + 0x80808080u;
-      v[2 * j + 1] = static_cast<uint32_t>(__float2int_rn(f1 * sc)) + 0x80808080u;
-    }
-  }
-  // gather byte p of the even and of the odd columns, then flip the top bit
-  // of each byte to get d_p
-  const uint32_t ae = prmt(v[0], v[2], 0x5140), be = prmt(v[4], v[6], 0x5140);
-  const uint32_t ao = prmt(v[1], v[3], 0x5140), bo = prmt(v[5], v[7], 0x5140);
-  const uint32_t ce = prmt(v[0], v[2], 0x7362), de = prmt(v[4], v[6], 0x7362);
-  const uint32_t co = prmt(v[1], v[3], 0x7362), dq = prmt(v[5], v[7], 0x7362);
-  uint32_t P[4][2];
-  P[0][0] = prmt(ae, be, 0x5410) ^ 0x80808080u;
-  P[0][1] = prmt(ao, bo, 0x5410) ^ 0x80808080u;
-  P[1][0] = prmt(ae, be, 0x7632) ^ 0x80808080u;
-  P[1][1] = prmt(ao, bo, 0x7632) ^ 0x80808080u;
-  P[2][0] = prmt(ce, de, 0x5410) ^ 0x80808080u;
-  P[2][1] = prmt(co, dq, 0x5410) ^ 0x80808080u;
-  P[3][0] = NP == 4 ? prmt(ce, de, 0x7632) ^ 0x80808080u : 0u;
-  P[3][1] = NP == 4 ? prmt(co, dq, 0x7632) ^ 0x80808080u : 0u;
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + (tp * 8 + gp) * 16), "r"(P[0][0]),
-               "r"(P[0][1]), "r"(P[1][0]), "r"(P[1][1])
-               : "memory");
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + 512 + (tp * 8 + gp) * 16), "r"(P[2][0]),
-               "r"(P[2][1]), "r"(P[3][0]), "r"(P[3][1])
-               : "memory");
-  G.q0 = __int_as_float((E + 3 - 8 * NP) << 23);                 // 2^(E - 124 - 8 NP)
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    int X = dp4a_us(0x01010101u, P[p][0], dp4a_us(0x01010101u, P[p][1], 0));
-    X += __shfl_xor_sync(0xffffffffu, X, 8);
-    X += __shfl_xor_sync(0xffffffffu, X, 16);                    // X_p of group gp (|X_p| <= 4096)
-    G.xq[p] = static_cast<float>(X) * __int_as_float((E + 3 - 8 * NP + 8 * p) << 23);   // exact
   }
 }
 
@@ -709,33 +554,6 @@ __device__ __forceinline__ float finish_rows(float (&yacc)[8], int lane, int& ro
 
 // --------------------------------------------------------------- kernel ----
 
-// Position of a chunk in the batch: item, index inside the item, tile row and
-// column.  Workers walk their ranges in order, so positions advance by one
-// without divisions.
-struct Pos {
-  int it;
-  int32_t tr, tc;
-  int64_t local;
-  template <class GemvArgs>
-  __device__ __forceinline__ void seek(const GemvArgs& a, int64_t c) {
-    int lo = 0, hi = a.nitems - 1;                  // last item with cbase <= c
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
-    }
-    it = lo;
-    local = c - a.items[it].cbase;
-    tr = static_cast<int32_t>(local / a.items[it].TC);
-    tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * a.items[it].TC);
-  }
-  template <class GemvArgs>
-  __device__ __forceinline__ void next(const GemvArgs& a) {
-    ++local;
-    if (++tc == a.items[it].TC) { tc = 0; ++tr; }
-    if (local == a.items[it].nchunks && it + 1 < a.nitems) { ++it; local = 0; tr = 0; tc = 0; }
-  }
-};
-
 // ----------------------------------------------------- segment results ----
 
 // End of a segment (item it, tile row tr) of warp w (range [lo, hi)); each
@@ -813,40 +631,6 @@ __device__ __forceinline__ int xslot_of(const Pos& p) {
   int d = p.tc - e.y;
   if (d < 0) d += e.w;
   return e.x + d;
-}
-
-__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// One x slice (its bf16 values in this prep lane's xr) into cache slot `sa`:
-// 3 or 4 digit planes (the most any of its groups needs), or the raw slice
-// for the binary32 path; the group records hold q0, xq0..xq3 and that mode.
-__device__ __forceinline__ void xslot_fill(const uint4 xr, uint32_t sa, int lane) {
-  const int gp = lane & 7, tp = lane >> 3;
-  int E;
-  const int need = __reduce_max_sync(0xffffffffu, q4_x_need(xr, E));
-  XGroup G = {};
-  if (need == 3) {
-    q4_x_planes<3>(xr, E, sa, lane, G);
-  } else if (need == 4) {
-    q4_x_planes<4>(xr, E, sa, lane, G);
-  } else {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sa + (tp * 8 + gp) * 16), "r"(xr.x), "r"(xr.y),
-                 "r"(xr.z), "r"(xr.w)
-                 : "memory");
-  }
-  if (tp == 0) {
-    const uint32_t gr = sa + kXSlotG + gp * 32;
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(gr), "f"(G.q0), "f"(G.xq[0]), "f"(G.xq[1]),
-                 "f"(G.xq[2])
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(gr + 16), "r"(__float_as_uint(G.xq[3])),
-                 "r"(static_cast<uint32_t>(need)), "r"(0u), "r"(0u)
-                 : "memory");
-  }
 }
 
 // Threads per CTA the kernel is compiled for.  One token: at most 128
@@ -1159,8 +943,7 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int
 
 template <int KIND, int MAXB, int MT>
 static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
-  const int slot = MT == 1 ? KIND + (MAXB == 1 ? 0 : MAXB == 8 ? 4 : 8) : (MT == 2 ? 20 : 24) + KIND;
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT>), slot);
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT>));
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: SMs freed by the previous grid start this
   // one at once; the kernel waits for the previous grid before touching x, y
@@ -1216,6 +999,14 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
                                      const DeviceInfo& info, const Top1Out* top1, cudaStream_t s) {
   GemvArgsT<MAXB> a;
   fill_items(a, items, n);
+  a.out_f32 = out_f32;
+  a.m = 1;
+  a.x_stride = 0;
+  a.y_stride = 0;
+  a.top1 = top1 != nullptr;
+  a.top1_idx = top1 ? top1->idx : nullptr;
+  a.top1_key_out = top1 ? top1->key : nullptr;
+  a.top1_row_base = top1 ? top1->row_base : 0u;
   GemvPlan p;
   if (!gemv_plan(kind, a.T, info, &p, 1)) return cudaErrorInvalidValue;
   fill_workspace(a, workspace);

@@ -16,8 +16,8 @@ struct DeviceInfo {
 cudaError_t device_info(DeviceInfo* out);
 
 // Raise a kernel's dynamic shared-memory limit to the device maximum once per
-// (device, slot); slots 0..31.
-cudaError_t set_max_dynamic_smem(const void* func, int slot);
+// (device, kernel).
+cudaError_t set_max_dynamic_smem(const void* func);
 
 // ---- GEMV (M = 1), a batch of independent items of one kind per launch ----
 constexpr int kMaxGemvItems = 256;

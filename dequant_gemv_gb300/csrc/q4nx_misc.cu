@@ -161,7 +161,7 @@ cudaError_t launch_decode(int kind, const void* chunks, int64_t TR, int64_t TC, 
       // persistent: as many CTAs as fit on the GPU at once, never more than chunks
       const void* f = kind == kQ8_KR ? reinterpret_cast<const void*>(decode_q8_kernel<kQ8_KR>)
                                      : reinterpret_cast<const void*>(decode_q8_kernel<kQ8_BLK>);
-      cudaError_t e = set_max_dynamic_smem(f, kind == kQ8_KR ? 29 : 30);
+      cudaError_t e = set_max_dynamic_smem(f);
       if (e != cudaSuccess) return e;
       int dev = 0, sms = 0, per_sm = 0;
       if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
