@@ -375,7 +375,7 @@ def test_argmax_signed_zeros_and_infs(q):
 
 
 def _ambiguous_and_check(idx_gpu, logits, w, kind, N, K, X, bar_rel, what):
-    """Reading o12: per row, the top-1 of the GPU logits must equal the top-1 of
+    """Reading o24: per row, the top-1 of the GPU logits must equal the top-1 of
     the binary64 oracle logits wherever the oracle's top-2 gap exceeds twice the
     bar.  Rows below that gap are ambiguous (several answers are within the
     bar): there the GPU's choice must be a row whose oracle logit lies within
