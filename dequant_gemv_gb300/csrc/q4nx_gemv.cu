@@ -45,8 +45,11 @@ __shared__ unsigned long long s_top1_key;
 // a launch then need no 64-bit division, which cost 0.3-0.7 us a launch on
 // that critical path.
 constexpr int kMaxGemvWarps = 16;          // warps per CTA the plan may choose (12 at most today)
-__shared__ uint32_t s_wlo[kMaxGemvWarps];
+__shared__ uint32_t s_wlo[kMaxGemvWarps + 1];     // [nwarps]: the CTA's chunk count
 __shared__ long long s_clast;
+// The CTA's range [Lc, Hc): kept here for the row sums, not in registers
+// across the main loop.
+__shared__ long long s_range[2];
 
 // x-slice cache (4-bit kinds, one token).  Every warp used to turn the x
 // slice of each chunk it read into digit planes, although the chunks of one
@@ -260,10 +263,18 @@ __device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, 
     s = bf16_bits_to_f32(L.f0[i]);
     z = bf16_bits_to_f32(L.f1[i]);
   } else {                                         // exact products: 8 x 6 significant bits
-    s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * static_cast<float>(L.f1[i] & 0xFFFFu);
-    z = bf16_bits_to_f32(L.f0[i] >> 16) * static_cast<float>(L.f1[i] >> 16);
+    // sc, mn < 64 as binary32: the bits of 2^23 + v, less 2^23
+    const float sc = __uint_as_float(0x4B000000u | (L.f1[i] & 0xFFFFu)) - 8388608.0f;
+    const float mn = __uint_as_float(0x4B000000u | (L.f1[i] >> 16)) - 8388608.0f;
+    s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * sc;
+    z = bf16_bits_to_f32(L.f0[i] >> 16) * mn;
   }
 }
+
+// 1.5 * 2^23 and its binary32 bits: for an integer |i| < 2^22 the bits
+// kMagicBits + i are the binary32 number kMagic + i.
+constexpr float kMagic = 12582912.0f;
+constexpr int kMagicBits = 0x4B400000;
 
 // One token's planes of this lane's group against two rows' codes: the
 // per-plane partials added to (acc.x, acc.y).
@@ -271,10 +282,14 @@ template <int KIND, int NP>
 __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uint32_t (&hi)[2][4], float2 s2,
                                            float2 z2, const uint4 (&PA)[4], const uint4 (&PB)[4], const XGroup& G,
                                            float2 acc) {
+  // Each accumulator starts at the bits of 1.5 * 2^23, so that, with |S_p| <
+  // 2^22, it ends as the binary32 number 1.5 * 2^23 + S_p exactly; one fma
+  // with the plane weight then gives S_p q_p exactly (no int-to-float
+  // conversion).
   int S[2][4];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+    int a0 = kMagicBits, a1 = kMagicBits, a2 = kMagicBits, a3 = kMagicBits;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       a0 = dp4a_us(lo[r][t], PA[t].x, a0);
@@ -297,9 +312,10 @@ __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uin
   for (int p = NP - 1; p >= 0; --p) {
     const float qp = G.q0 * static_cast<float>(1 << (8 * p));        // exact power of two
     const float2 qq = make_float2(qp, qp);
+    const float2 mq = make_float2(-kMagic * qp, -kMagic * qp);
     const float2 xq = make_float2(G.xq[p], G.xq[p]);
-    // exact: |S_p| < 2^24 times a power of two
-    const float2 sq = fmul2(make_float2(__int2float_rn(S[0][p]), __int2float_rn(S[1][p])), qq);
+    // exact: (1.5 * 2^23 + S_p) q_p - 1.5 * 2^23 q_p = S_p q_p, |S_p| < 2^22 times a power of two
+    const float2 sq = ffma2(make_float2(__int_as_float(S[0][p]), __int_as_float(S[1][p])), qq, mq);
     if constexpr (KIND == kQ4_1) {
       const float2 zx = fmul2(z2, xq);                          // exact: 8 x 13 significant bits
       acc = fadd2(acc, ffma2(s2, sq, zx));
@@ -440,32 +456,28 @@ __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scr
   __syncwarp();                                                 // scratch is rewritten by the next chunk
 }
 
-// One chunk, x prepared here: each token's slice becomes digit planes in the
-// warp's scratch (3 or 4 planes, the most any token's groups need), or, when
-// some group spans more than 32-bit fixed point holds, the raw slices go to
-// the scratch for the binary32 path.
+// One chunk's x, prepared by the warp: each token's slice becomes digit
+// planes in the warp's scratch (3 or 4 planes, the most any token's groups
+// need), or, when some group spans more than 32-bit fixed point holds, the
+// raw slices go to the scratch for the binary32 path.  Returns that mode (3,
+// 4 or 5); the caller syncs the warp before the scratch is read.
 template <int KIND, int MT>
-__device__ __forceinline__ void q4_compute(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
-                                           float (&yacc)[MT][8]) {
+__device__ __forceinline__ int q4_prep(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
+                                       XGroup (&G)[MT]) {
   int E[MT];
   int need = 3;
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok)
     if (tok < m) need = max(need, q4_x_need(L.xr[tok], E[tok]));
   need = __reduce_max_sync(0xffffffffu, need);
-  XGroup G[MT];
   if (need == 3) {
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok)
       if (tok < m) q4_x_planes<3>(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
-    __syncwarp();
-    q4_fixed<KIND, MT, 3>(L, scratch, lane, m, G, yacc);
   } else if (need == 4) {
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok)
       if (tok < m) q4_x_planes<4>(L.xr[tok], E[tok], scratch + tok * kScratchBytes, lane, G[tok]);
-    __syncwarp();
-    q4_fixed<KIND, MT, 4>(L, scratch, lane, m, G, yacc);
   } else {
     const int gp = lane & 7, tp = lane >> 3;
 #pragma unroll
@@ -474,9 +486,18 @@ __device__ __forceinline__ void q4_compute(const Q4Lane<KIND, MT>& L, uint32_t s
         asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(scratch + tok * kScratchBytes + (tp * 8 + gp) * 16),
                      "r"(L.xr[tok].x), "r"(L.xr[tok].y), "r"(L.xr[tok].z), "r"(L.xr[tok].w)
                      : "memory");
-    __syncwarp();
-    q4_float<KIND, MT>(L, scratch, lane, m, yacc);
   }
+  return need;
+}
+
+// One chunk's arithmetic, its x prepared in `src` (the warp's scratch or a
+// cache slot) in the given mode (uniform over the warp).
+template <int KIND, int MT>
+__device__ __forceinline__ void q4_math(const Q4Lane<KIND, MT>& L, uint32_t src, int lane, int m, int mode,
+                                        const XGroup (&G)[MT], float (&yacc)[MT][8]) {
+  if (mode == 3) q4_fixed<KIND, MT, 3>(L, src, lane, m, G, yacc);
+  else if (mode == 4) q4_fixed<KIND, MT, 4>(L, src, lane, m, G, yacc);
+  else q4_float<KIND, MT>(L, src, lane, m, yacc);
 }
 
 // Q8: lane covers rows 8*qe + (0..7) of columns 8t + kc, t = 0..31.
@@ -564,11 +585,12 @@ __device__ __forceinline__ float finish_rows(float (&yacc)[8], int lane, int& ro
 // slots in warp order and stores y, or hands the row on to cross_cta_row when
 // other CTAs share it too.
 template <int MT, class GemvArgs>
-__device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int64_t Lc, int64_t Hc, int w, int nw,
-                                            int64_t lo, int64_t hi, int it, int64_t tr, int row,
+__device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int w, int nw, int it, int64_t tr, int row,
                                             const float (&val)[MT], float* slots, uint32_t* cnt, int lane) {
   const GemvItemDev& item = a.items[it];
   const int m = (MT == 1) ? 1 : a.m;
+  const int64_t Lc = s_range[0], Hc = s_range[1];
+  const int64_t lo = Lc + s_wlo[w], hi = Lc + s_wlo[w + 1];      // this warp's range
   const int64_t r0 = item.cbase + tr * item.TC, r1 = r0 + item.TC;
   if (lo <= r0 && r1 <= hi) {
 #pragma unroll
@@ -615,11 +637,11 @@ __device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, uin
                                             uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
   mbar_arrive_expect_tx(bar, CB + xbytes);
-  bulk_g2s(dst, a.items[p.it].chunks + p.local * CB, CB, bar);
+  bulk_g2s(dst, p.w, CB, bar);
 }
 template <int KIND, int MT, class GemvArgs>
 __device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
-  const uint8_t* x = a.items[p.it].x + static_cast<int64_t>(p.tc) * kXSliceBytes;
+  const uint8_t* x = p.x;
 #pragma unroll
   for (int tok = 0; tok < MT; ++tok)
     if (tok < m) bulk_g2s(dst + tok * kXSliceBytes, x + tok * a.x_stride, kXSliceBytes, bar);
@@ -672,7 +694,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur{}, pre{};                         // chunk being processed / next chunk to fetch
-  cur.seek(a, lo);
+  cur.seek<CB>(a, lo);
   pre = cur;
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
@@ -682,7 +704,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     Pos p = pre;
     for (int s = 0; s < stages && s < n; ++s) {
       issue_chunk<KIND, MT>(a, p, static_cast<uint32_t>(m * kXSliceBytes), ring + s * CB, &bars[s]);
-      p.next(a);
+      p.next<CB>(a);
     }
   }
   if (XC && a.xslots > 0 && threadIdx.x == 32 * (nwarps - 1)) {
@@ -690,8 +712,8 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     // used when they fit and each is reused four times on average (below
     // that, filling it costs the short launches more than it saves)
     Pos p0{}, p1{};
-    p0.seek(a, Lc);
-    p1.seek(a, Hc - 1);
+    p0.seek<CB>(a, Lc);
+    p1.seek<CB>(a, Hc - 1);
     int ok = p1.it - p0.it < kXTabItems, total = 0;
     for (int it = p0.it; ok && it <= p1.it; ++it) {
       const GemvItemDev& I = a.items[it];
@@ -708,10 +730,14 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     s_xinfo[2] = total;
     s_xinfo[3] = p1.it - p0.it + 1;
   }
-  if (warp == 0 && lane < nwarps) s_wlo[lane] = static_cast<uint32_t>(((Hc - Lc) * lane) / nwarps);
+  if (warp == 0 && lane <= nwarps) s_wlo[lane] = static_cast<uint32_t>(((Hc - Lc) * lane) / nwarps);
+  if (threadIdx.x == 0) {
+    s_range[0] = Lc;
+    s_range[1] = Hc;
+  }
   if (threadIdx.x == blockDim.x - 1) {
     Pos e{};
-    e.seek(a, Hc - 1);
+    e.seek<CB>(a, Hc - 1);
     const int64_t r1 = a.items[e.it].cbase + (static_cast<int64_t>(e.tr) + 1) * a.items[e.it].TC;
     s_clast = r1 > Hc ? cta_of(r1 - 1, a.T, a.grid) : b;
   }
@@ -725,12 +751,11 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   const bool xc = XC && a.xslots > 0 && s_xinfo[0] != 0;      // this CTA's x slices come from the cache
   const uint32_t xbytes = xc ? 0u : static_cast<uint32_t>(m * kXSliceBytes);   // x bytes with each refill
   asm volatile("griddepcontrol.wait;" ::: "memory");            // x, y and the workspace may be the previous grid's
-  if (lane == 0) {
-    // the x slices of the chunks already in flight (unused when the cache serves them)
-    for (int s = 0; s < stages && s < n; ++s) {
-      issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
-      pre.next(a);
-    }
+  // the x slices of the chunks already in flight (unused when the cache
+  // serves them); every lane walks `pre`, so that it stays warp-uniform
+  for (int s = 0; s < stages && s < n; ++s) {
+    if (lane == 0) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
+    pre.next<CB>(a);
   }
   if (xc) {
     // fill the cache: warp w prepares slices w, w + nwarps, ...; each lane
@@ -779,7 +804,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       float v[MT];
 #pragma unroll
       for (int tok = 0; tok < MT; ++tok) v[tok] = finish_rows<KIND>(yacc[tok], lane, row);
-      finish_segment<MT>(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
+      finish_segment<MT>(a, b, warp, nwarps, seg_it, seg_tr, row, v, slots, cnt, lane);
 #pragma unroll
       for (int tok = 0; tok < MT; ++tok)
 #pragma unroll
@@ -789,36 +814,43 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     }
     const uint32_t st = smem_u32(ring + s * CB);
     const uint32_t xs = smem_u32(xsl + s * MT * kXSliceBytes);
-    // 4-bit chunks: the lanes take their share of the stage into registers
-    // and the stage is refilled before the arithmetic; Q8: after it
+    // 4-bit chunks: the lanes take their share of the stage into registers,
+    // find or prepare the chunk's x (which covers the loads' latency), and
+    // the stage is refilled before the arithmetic; Q8: after it
     Q4Lane<Q4 ? KIND : kQ4_1, MT> q4l;
-    if constexpr (Q4) q4_read<KIND, MT>(st, xs, !xc, lane, m, q4l);
-    else q8_chunk<KIND, MT>(st, xs, lane, m, yacc);
-    __syncwarp();
-    if (lane == 0 && j + stages < n) {
-      issue_chunk<KIND, MT>(a, pre, xbytes, ring + s * CB, &bars[s]);
-      if (!xc) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
-      pre.next(a);
-    }
+    XGroup G[MT];
+    int mode = 0;
+    uint32_t src = scratch;
     if constexpr (Q4) {
+      q4_read<KIND, MT>(st, xs, !xc, lane, m, q4l);
       if (XC && xc) {
-        const uint32_t sa = xcache + xslot_of(cur) * kXSlotBytes;
-        const uint32_t gr = sa + kXSlotG + (lane & 7) * 32;
+        src = xcache + xslot_of(cur) * kXSlotBytes;
+        const uint32_t gr = src + kXSlotG + (lane & 7) * 32;
         const uint4 g0 = lds128(gr), g1 = lds128(gr + 16);
-        XGroup G[MT];
         G[0].q0 = __uint_as_float(g0.x);
         G[0].xq[0] = __uint_as_float(g0.y);
         G[0].xq[1] = __uint_as_float(g0.z);
         G[0].xq[2] = __uint_as_float(g0.w);
         G[0].xq[3] = __uint_as_float(g1.x);
-        if (g1.y == 3u) q4_fixed<KIND, MT, 3>(q4l, sa, lane, m, G, yacc);        // (the slice's mode: uniform)
-        else if (g1.y == 4u) q4_fixed<KIND, MT, 4>(q4l, sa, lane, m, G, yacc);
-        else q4_float<KIND, MT>(q4l, sa, lane, m, yacc);
+        mode = static_cast<int>(g1.y);                          // the slice's mode: uniform
       } else {
-        q4_compute<KIND, MT>(q4l, scratch, lane, m, yacc);
+        mode = q4_prep<KIND, MT>(q4l, scratch, lane, m, G);
       }
+    } else {
+      q8_chunk<KIND, MT>(st, xs, lane, m, yacc);
     }
-    cur.next(a);
+    // every lane's reads of the stage are done before it is refilled, and
+    // the prepared planes are visible to the warp
+    __syncwarp();
+    if (j + stages < n) {
+      if (lane == 0) {
+        issue_chunk<KIND, MT>(a, pre, xbytes, ring + s * CB, &bars[s]);
+        if (!xc) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
+      }
+      pre.next<CB>(a);
+    }
+    if constexpr (Q4) q4_math<KIND, MT>(q4l, src, lane, m, mode, G, yacc);
+    cur.next<CB>(a);
     if (++s == stages) s = 0;
   }
   if (failed) {
@@ -830,7 +862,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     float v[MT];
 #pragma unroll
     for (int tok = 0; tok < MT; ++tok) v[tok] = finish_rows<KIND>(yacc[tok], lane, row);
-    finish_segment<MT>(a, b, Lc, Hc, warp, nwarps, lo, hi, seg_it, seg_tr, row, v, slots, cnt, lane);
+    finish_segment<MT>(a, b, warp, nwarps, seg_it, seg_tr, row, v, slots, cnt, lane);
   }
   if (MT == 1 && a.top1) {
     // every warp's rows are folded in; the CTA's key goes to the launch's key,

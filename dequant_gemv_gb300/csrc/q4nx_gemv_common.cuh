@@ -176,30 +176,52 @@ __device__ __forceinline__ void q4_x_planes(const uint4 xr, int E, uint32_t scra
 }
 
 
-// Position of a chunk in the batch: item, index inside the item, tile row and
-// column.  Workers walk their ranges in order, so positions advance by one
-// without divisions.
+// Position of a chunk in the batch: item, tile row and column, with the
+// chunk's address and its x slice's, and the item's tile columns and chunks
+// left.  Workers walk their ranges in order, so a position advances by one
+// chunk with pointer increments; the item table (kernel parameters, read with
+// a dynamic index) is read only when the walk enters the next item.
 struct Pos {
   int it;
   int32_t tr, tc;
-  int64_t local;
-  template <class GemvArgs>
+  int32_t TC;
+  int32_t left;                     // chunks of the item from this one to its end (tile counts fit 31 bits)
+  const uint8_t* w;                 // this chunk
+  const uint8_t* x;                 // the x slice of its tile column (token 0)
+  template <int CB, class GemvArgs>
+  __device__ __forceinline__ void enter(const GemvArgs& a, int item, int64_t local) {
+    const GemvItemDev& I = a.items[item];
+    it = item;
+    TC = I.TC;
+    left = static_cast<int32_t>(I.nchunks - local);
+    tr = static_cast<int32_t>(local / TC);
+    tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * TC);
+    w = I.chunks + local * CB;
+    x = I.x + static_cast<int64_t>(tc) * kXSliceBytes;
+  }
+  template <int CB, class GemvArgs>
   __device__ __forceinline__ void seek(const GemvArgs& a, int64_t c) {
     int lo = 0, hi = a.nitems - 1;                  // last item with cbase <= c
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
     }
-    it = lo;
-    local = c - a.items[it].cbase;
-    tr = static_cast<int32_t>(local / a.items[it].TC);
-    tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * a.items[it].TC);
+    enter<CB>(a, lo, c - a.items[lo].cbase);
   }
-  template <class GemvArgs>
+  template <int CB, class GemvArgs>
   __device__ __forceinline__ void next(const GemvArgs& a) {
-    ++local;
-    if (++tc == a.items[it].TC) { tc = 0; ++tr; }
-    if (local == a.items[it].nchunks && it + 1 < a.nitems) { ++it; local = 0; tr = 0; tc = 0; }
+    w += CB;
+    x += kXSliceBytes;
+    if (++tc == TC) { tc = 0; ++tr; x -= static_cast<int64_t>(TC) * kXSliceBytes; }
+    if (--left == 0 && it + 1 < a.nitems) {                         // the next item's first chunk
+      const GemvItemDev& I = a.items[++it];
+      TC = I.TC;
+      left = static_cast<int32_t>(I.nchunks);
+      tr = 0;
+      tc = 0;
+      w = I.chunks;
+      x = I.x;
+    }
   }
 };
 
