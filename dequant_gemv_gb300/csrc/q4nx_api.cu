@@ -255,8 +255,8 @@ int q4nx_gemv_top1_key(const q4nx_weight* w, const void* x_dev, int64_t row_base
                                     info, static_cast<cudaStream_t>(stream)));
 }
 
-// Workspace of q4nx_gemm_m64: the GEMM's part (error word, posting counters,
-// partial tiles; partial tiles stay behind after a call) followed by the
+// Workspace of q4nx_gemm_m64: the GEMM's part (error word, partial tiles,
+// posting counters; partial tiles stay behind after a call) followed by the
 // few-token GEMV's part (posted row sums, left zero-filled).  Both share the
 // error word at offset 0, and one size serves every M.
 static uint64_t gemm_part_bytes(const q4nx_weight* w) {

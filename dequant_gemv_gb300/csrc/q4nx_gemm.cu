@@ -135,6 +135,9 @@ static_assert(kDequantWarps == 8, "dequant warps: two per TMEM lane quarter");
 // tcgen05 instruction descriptor: D fp32, A bf16, B bf16, both K-major, N = 64, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kTileN >> 3) << 17) | ((kTileM >> 4) << 24);
 
+// Workspace bytes of the partial tiles: one per CTA, at most 1024 CTAs.
+constexpr uint64_t kPartialBytes = static_cast<uint64_t>(1024) * kTileN * kTileM * 4;
+
 struct Args {
   const uint8_t* chunks;
   void* Y;
@@ -800,9 +803,13 @@ uint64_t gemm_workspace_bytes(int64_t TR, int64_t TC, int M) {
   (void)TC;
   (void)M;
   const int64_t tiles = (TR + 3) / 4;
-  // error word, posting counters, one partial tile per CTA (at most 1024 CTAs)
-  return kWsErrBytes + align16(static_cast<uint64_t>(tiles) * 4) +
-         static_cast<uint64_t>(1024) * gemm::kTileN * gemm::kTileM * 4;
+  // error word, one partial tile per CTA (at most 1024 CTAs), posting
+  // counters.  The partials come first: their region has the same place and
+  // size for every weight, and the regions whose place depends on the weight
+  // (the counters, and the few-token GEMV's part after them) are left
+  // zero-filled by every call, so weights of different sizes can share one
+  // workspace without stale partials reaching another weight's counters.
+  return kWsErrBytes + gemm::kPartialBytes + align16(static_cast<uint64_t>(tiles) * 4);
 }
 
 namespace {
@@ -877,8 +884,8 @@ cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void
   a.Y = Y;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.err = reinterpret_cast<uint32_t*>(ws);
-  a.counters = reinterpret_cast<uint32_t*>(ws + kWsErrBytes);
-  a.partials = reinterpret_cast<float*>(ws + kWsErrBytes + align16(static_cast<uint64_t>(tiles) * 4));
+  a.partials = reinterpret_cast<float*>(ws + kWsErrBytes);
+  a.counters = reinterpret_cast<uint32_t*>(ws + kWsErrBytes + gemm::kPartialBytes);
   a.TR = TR;
   a.TC = TC;
   a.N = TR * 32;

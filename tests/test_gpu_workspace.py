@@ -100,12 +100,45 @@ def _planted_gemm(q):
     return w, X, W, Xd, need
 
 
+def test_gemm_weights_of_different_sizes_share_one_workspace(q):
+    """One GEMM workspace, sized for the largest, serves weights with
+    different tile counts one after another, tensor-core blocks and
+    few-token calls alike: the regions whose place depends on the weight (the
+    posting counters, the few-token part) are left zero-filled, so the
+    partial tiles that one weight's calls leave behind never reach another
+    weight's counters."""
+    shapes = [(synth.Q4_1, 1024, 4096, 64), (synth.Q4_1, 12288, 4096, 64), (synth.Q4_1, 4096, 1536, 2),
+              (synth.Q4_1, 640, 12288, 33), (synth.Q4_1, 12288, 4096, 64), (synth.Q4_1, 2048, 2560, 2)]
+    made = []
+    for i, (kind, N, K, M) in enumerate(shapes):
+        f, w = synth.make(kind, N, K, synth.rng(23, 50 + i, 0))
+        X = synth.activations(synth.rng(23, 60 + i, 0), M, K)
+        W = q.Weight(torch.from_numpy(w).to(DEV), kind, N, K)
+        Xd = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).to(DEV).view(torch.bfloat16)
+        made.append((kind, N, K, M, w, X, W, Xd))
+    need = max(int(q.lib.q4nx_gemm_workspace(ctypes.byref(W.c()), M)) for (_, _, _, M, _, _, W, _) in made)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for kind, N, K, M, w, X, W, Xd in made:
+        Y = q.q4nx_gemm_m64(W, Xd, out_dtype="f32", ws=ws).cpu().numpy().astype(np.float64)
+        q.q4nx_check(ws)
+        rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(N - 64, N),
+                                         np.random.default_rng(N + K).integers(0, N, 128)]))
+        Y64, A = oracle.matmul(w, kind, N, K, X, rows=rows)
+        bar = 1e-3 if M <= 2 else 1e-3 + 2.0 ** -9                 # CUDA-core / tensor-core path
+        assert np.all(np.abs(Y[:, rows] - Y64) <= bar * A), (N, K, M)
+
+
+# GEMM workspace: a 16-byte error block, the partial tiles (one per CTA, at
+# most 1024 CTAs, each 64 tokens x 128 rows of fp32), then the posting
+# counters (one per tile).
+GEMM_COUNTERS = 16 + 1024 * 64 * 128 * 4
+
+
 def _plant(ws):
-    """Tile 0's posting counter (the u32 after the 16-byte error block) far
-    above any count its contributors can reach: the finisher's wait cannot
-    succeed."""
+    """Tile 0's posting counter far above any count its contributors can
+    reach: the finisher's wait cannot succeed."""
     ws.zero_()
-    ws[16:20] = torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8, device=ws.device)
+    ws[GEMM_COUNTERS:GEMM_COUNTERS + 4] = torch.tensor([0, 0, 0, 0x40], dtype=torch.uint8, device=ws.device)
 
 
 def test_gemm_bounded_wait_reports_timeout_and_recovers(q):
