@@ -914,9 +914,10 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
   // dependent launch) starts its weight copies on the same SMs while this one
   // drains -- back-to-back GEMVs then overlap their start-up latency.  Q8
   // chunks are larger and gain more from a deeper ring than from that overlap.
-  // (less 512 bytes for the kernel's static shared memory, 256 bytes today:
-  // two CTAs of a two-per-SM launch must both fit, or its cross-CTA row sums
-  // would wait on a CTA that has no SM)
+  // (less 512 bytes for the kernel's static shared memory, 384 bytes today:
+  // two CTAs of a two-per-SM launch should both fit.  That is for speed, not
+  // for progress: a finisher waits only on higher-indexed CTAs, which post
+  // after their first tile row, so in-order dispatch suffices)
   // Several tokens need more registers than two CTAs per SM leave, so those
   // launches take the whole of the shared memory.
   const uint64_t cap =
