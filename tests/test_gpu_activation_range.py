@@ -17,8 +17,12 @@ Cases:
     the binary32 / bf16 spacing there, and no cosine is taken);
   * groups whose magnitudes span exactly 2^14 and just beyond;
   * every weight an exact zero: the output is exactly zero;
-  * scales near 2^+-100.
-Every output is checked against the binary64 oracle at 1e-3 * sum_k |w_k x_k|.
+  * scales near 2^+-100;
+  * one +Inf, -Inf or NaN activation (GEMV of every kind, the batched layer
+    on the x-slice cache path, the tensor-core GEMM): each row meets the
+    special value exactly as the binary64 sum does (0 * Inf = NaN).
+Every finite output is checked against the binary64 oracle at
+1e-3 * sum_k |w_k x_k|.
 """
 import numpy as np
 import pytest
@@ -274,3 +278,102 @@ def test_cached_x_slices_many_items_per_cta(q):
     for (W, xt, y), (w, x, N, K) in zip(items, refs):
         Y64, A = oracle.matmul(w, synth.Q4_1, N, K, x)
         assert_within(out_values(y), Y64, A, False, f"batch item {N}x{K}")
+
+
+# ------------------------------------------------- Inf and NaN activations --
+
+def special_x(K: int, which: str, col: int, seed: int) -> np.ndarray:
+    """N(0, 1) activations with one +Inf, -Inf or NaN at column `col`."""
+    x = synth.activations(synth.rng(49, seed), 1, K)[0].copy()
+    x[col] = {"+inf": 0x7F80, "-inf": 0xFF80, "nan": 0x7FC0}[which]
+    return x
+
+
+def assert_same_specials(y, Y64, what):
+    """IEEE outcome, row by row: NaN where the binary64 sum is NaN, an
+    infinity of the same sign where it is infinite, nothing else."""
+    y, Y64 = np.asarray(y, np.float64), np.asarray(Y64, np.float64)
+    assert np.array_equal(np.isnan(y), np.isnan(Y64)), f"{what}: NaN pattern"
+    inf = np.isinf(Y64)
+    assert np.array_equal(np.isinf(y), inf), f"{what}: infinity pattern"
+    assert np.array_equal(np.sign(y[inf]), np.sign(Y64[inf])), f"{what}: infinity signs"
+    assert np.all(np.isnan(Y64) | inf), f"{what}: every row meets the special value"
+
+
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K, synth.Q8_KR])
+@pytest.mark.parametrize("which", ["+inf", "-inf", "nan"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_inf_and_nan_activations(q, kind, which, out):
+    """One infinite or NaN activation: a row's sum is +-Inf where its weight
+    at that column is nonzero (sign of the product), NaN where that weight is
+    exactly zero (0 * Inf) or the activation is NaN, as in binary64."""
+    N, K = 2048, 2560
+    f, w = synth.make(kind, N, K, synth.rng(49, kind, 1))
+    x = special_x(K, which, 1337, kind)
+    W = q.Weight(to_dev_bytes(w), kind, N, K)
+    y = out_values(q.q4nx_gemv(W, to_dev_bf16(x), out_dtype=out))
+    Y64, _ = oracle.matmul(w, kind, N, K, x)
+    assert_same_specials(y, Y64, f"kind {kind} {which} {out}")
+
+
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K])
+def test_infinity_on_exact_zero_weights(q, kind):
+    """Q4_0-mapped weights (code 8 = an exact zero weight in every group's
+    first column) with +Inf there: every row is 0 * Inf = NaN."""
+    N, K = 1024, 1024
+    f, w = q4_0_mapped_weight(kind, N, K, seed=3)
+    x = special_x(K, "+inf", 256, 7)
+    W = q.Weight(to_dev_bytes(w), kind, N, K)
+    y = out_values(q.q4nx_gemv(W, to_dev_bf16(x), out_dtype="f32"))
+    Y64, _ = oracle.matmul(w, kind, N, K, x)
+    assert np.all(np.isnan(Y64))
+    assert_same_specials(y, Y64, f"kind {kind} Inf on zero weights")
+
+
+def test_decode_layer_batch_with_inf_and_nan(q):
+    """The seven projections of a layer in one launch (the x-slice cache
+    path): q's activations hold a +Inf, v's a NaN, the others are N(0, 1)
+    and stay within the bar."""
+    items, refs = [], []
+    for mi, (_, N, K) in enumerate(synth.QWEN3_06B_LAYER):
+        f, w = synth.workload_weight(2, mi, layer=6)
+        if mi == 0:
+            x = special_x(K, "+inf", 700, 30)
+        elif mi == 2:
+            x = special_x(K, "nan", 5, 31)
+        else:
+            x = synth.activations(synth.rng(49, 40 + mi), 1, K)[0]
+        y = torch.empty(N, dtype=torch.float32, device=DEV)
+        items.append((q.Weight(to_dev_bytes(w), synth.Q4_1, N, K), to_dev_bf16(x), y))
+        refs.append((mi, w, x, N, K))
+    q.q4nx_gemv_batch(items, out_dtype="f32")
+    for (W, xt, y), (mi, w, x, N, K) in zip(items, refs):
+        Y64, A = oracle.matmul(w, synth.Q4_1, N, K, x)
+        if mi in (0, 2):
+            assert_same_specials(out_values(y), Y64, f"layer matrix {mi}")
+        else:
+            assert_within(out_values(y), Y64, A, False, f"layer matrix {mi} beside special values")
+
+
+def test_gemm_64_tokens_with_inf_and_nan(q):
+    """The tensor-core GEMM: one token with a +Inf activation, one with a
+    NaN; those tokens' rows meet the special value as in binary64 (on the
+    bf16 weights the tensor cores multiply), the other tokens stay within
+    the tensor-core bar."""
+    N, K, M = 4096, 4096, 64
+    f, w = synth.make(synth.Q4_1, N, K, synth.rng(49, 50))
+    X = synth.activations(synth.rng(49, 51), M, K).copy()
+    X[5, 1000] = 0x7F80
+    X[9, 3] = 0x7FC0
+    W = q.Weight(to_dev_bytes(w), synth.Q4_1, N, K)
+    Y = q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype="f32").cpu().numpy().astype(np.float64)
+    rows = np.unique(np.concatenate([np.arange(0, 256), np.random.default_rng(5).integers(0, N, 512)]))
+    # (a weight's sign, and whether it is exactly zero, survive its bf16
+    # rounding, so the binary64 pattern on the exact weights is the one the
+    # tensor cores must give)
+    Ys, _ = oracle.matmul(w, synth.Q4_1, N, K, X[[5, 9]], rows=rows)
+    for i, m in enumerate((5, 9)):
+        assert_same_specials(Y[m, rows], Ys[i], f"token {m}")
+    others = [m for m in range(M) if m not in (5, 9)]
+    Y64, A = oracle.matmul(w, synth.Q4_1, N, K, X[others], rows=rows)
+    assert np.all(np.abs(Y[others][:, rows] - Y64) <= (1e-3 + 2.0 ** -9) * A)
