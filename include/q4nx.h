@@ -103,6 +103,10 @@ int q4nx_decode(const q4nx_weight* w, void* out_dev, uint64_t out_bytes, void* s
  * again (after Q4NX_E_DEVICE_TIMEOUT it must be zero-filled anew).  It holds
  * an error word and the partial sums of tile rows split between CTAs, each
  * posted with a ready flag (16 B + 256 KiB for any weight).
+ * Non-finite activations give each row the IEEE outcome of the sum (+-Inf,
+ * or NaN for 0*Inf or a NaN activation); chunks whose scale or zero fields
+ * are non-finite give non-finite rows, but not necessarily the per-weight
+ * pattern of Inf and NaN (decode such chunks with q4nx_decode instead).
  * Results are deterministic: partials are added in a fixed order.  A tile row
  * split between CTAs is finished by the CTA that holds its first chunk once
  * the later CTAs (at most two per SM) have posted; they get SMs as soon as
