@@ -9,7 +9,10 @@
 //
 // Design (HBM-bound: 0.625 B/weight for q4_1):
 //  * Persistent grid, one CTA per SM (two for 4-bit launches of 128 chunks or
-//    more per SM, each within half an SM).  The chunks of all items form one index
+//    more per SM, each within half an SM).  One-token 4-bit launches of at most
+//    8 chunks per SM (the projections of a small decode layer) take quarters
+//    of chunks (8 rows) as units, up to 16 warps per CTA: a warp's arithmetic
+//    on a whole chunk would otherwise be the launch's critical path.  The chunks of all items form one index
 //    space (item after item, each row-major over its tile grid); CTA b owns an
 //    even contiguous share, each warp a contiguous part of it.  A range is a
 //    run of (item, tile row) segments.
@@ -233,8 +236,10 @@ struct Q4Lane {
   uint32_t f0[8], f1[8];           // q4_1: scale, zero bits; Q4_K: S bits | M bits << 16, sc | mn << 16
 };
 
-template <int KIND, int MT>
-__device__ __forceinline__ void q4_read(uint32_t st, uint32_t xs, bool with_x, int lane, int m, Q4Lane<KIND, MT>& L) {
+// QTR: only quarter h's rows 8h + qr and 8h + 4 + qr, into entries 0 and 1.
+template <int KIND, int MT, bool QTR = false>
+__device__ __forceinline__ void q4_read(uint32_t st, uint32_t xs, bool with_x, int lane, int m, Q4Lane<KIND, MT>& L,
+                                        int h = 0) {
   const int gp = lane & 7, tp = lane >> 3;
   if (with_x) {
 #pragma unroll
@@ -243,8 +248,8 @@ __device__ __forceinline__ void q4_read(uint32_t st, uint32_t xs, bool with_x, i
   }
   const int qr = lane >> 3, g = lane & 7;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + qr;
+  for (int i = 0; i < (QTR ? 2 : 8); ++i) {
+    const int r = QTR ? 8 * h + 4 * i + qr : 4 * i + qr;
     L.cw[i] = lds128(st + r * 128 + g * 16);
     if constexpr (KIND == kQ4_1) {
       L.f0[i] = lds_u16(st + kQ41Scale + (r * 8 + g) * 2);
@@ -268,6 +273,17 @@ __device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, 
     const float mn = __uint_as_float(0x4B000000u | (L.f1[i] >> 16)) - 8388608.0f;
     s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * sc;
     z = bf16_bits_to_f32(L.f0[i] >> 16) * mn;
+  }
+}
+
+// A quarter's two row sums into the lane's accumulators of rows 4(2h) + qr
+// and 4(2h + 1) + qr (h is the same for the whole warp).
+__device__ __forceinline__ void add_quarter(float (&y)[8], int h, float a, float b) {
+  switch (h) {
+    case 0: y[0] += a; y[1] += b; break;
+    case 1: y[2] += a; y[3] += b; break;
+    case 2: y[4] += a; y[5] += b; break;
+    default: y[6] += a; y[7] += b; break;
   }
 }
 
@@ -330,9 +346,9 @@ __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uin
 
 // The exact-integer path for one chunk: rows 4i + qr of group g, every token,
 // NP digit planes per token in `scratch` (token stride kScratchBytes).
-template <int KIND, int MT, int NP>
+template <int KIND, int MT, int NP, bool QTR = false>
 __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
-                                         const XGroup (&G)[MT], float (&yacc)[MT][8]) {
+                                         const XGroup (&G)[MT], float (&yacc)[MT][8], int h = 0) {
   const int g = lane & 7;
   auto load_planes = [&](int tok, uint4 (&PA)[4], uint4 (&PB)[4]) {
 #pragma unroll
@@ -346,7 +362,28 @@ __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scr
       }
     }
   };
-  if constexpr (MT == 1) {
+  if constexpr (QTR) {
+    // one quarter: its two rows (entries 0 and 1) are rows 4(2h) + qr and
+    // 4(2h + 1) + qr of the chunk, accumulated in yacc[0][2h], yacc[0][2h + 1]
+    static_assert(MT == 1, "quarters: one token");
+    uint4 PA[4], PB[4];
+    load_planes(0, PA, PB);
+    float s[2], z[2];
+    uint32_t lo[2][4], hi[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      q4_scale_zero(L, r, s[r], z[r]);
+      const uint32_t w[4] = {L.cw[r].x, L.cw[r].y, L.cw[r].z, L.cw[r].w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        lo[r][t] = w[t] & 0x0F0F0F0Fu;
+        hi[r][t] = (w[t] >> 4) & 0x0F0F0F0Fu;
+      }
+    }
+    const float2 acc = q4_rows2<KIND, NP>(lo, hi, make_float2(s[0], s[1]), make_float2(z[0], z[1]), PA, PB, G[0],
+                                          make_float2(0.f, 0.f));
+    add_quarter(yacc[0], h, acc.x, acc.y);
+  } else if constexpr (MT == 1) {
     uint4 PA[4], PB[4];
     load_planes(0, PA, PB);
 #pragma unroll
@@ -409,9 +446,9 @@ __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scr
 // The binary32 path for one chunk (x groups that 32-bit fixed point does not
 // hold): every weight formed as fl(c s + z) and multiplied by x in an fma.
 // The raw bf16 x slices are in region A of `scratch`, [t][g] 16 B.
-template <int KIND, int MT>
+template <int KIND, int MT, bool QTR = false>
 __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
-                                         float (&yacc)[MT][8]) {
+                                         float (&yacc)[MT][8], int h = 0) {
   const int g = lane & 7;
   const float2 magic = make_float2(-8388608.0f, -8388608.0f);   // 2^23: float(2^23 + c) - 2^23 = c exactly
 #pragma unroll 1
@@ -427,7 +464,7 @@ __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scr
     }
     float part[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < (QTR ? 2 : 8); ++i) {
       float s, z;
       q4_scale_zero(L, i, s, z);
       const float2 s2 = make_float2(s, s), z2 = make_float2(z, z);
@@ -447,11 +484,15 @@ __device__ __forceinline__ void q4_float(const Q4Lane<KIND, MT>& L, uint32_t scr
     }
     // (tok is a loop variable: select the token's accumulators by comparison,
     // so that they stay in registers)
+    if constexpr (QTR) {
+      add_quarter(yacc[0], h, part[0], part[1]);
+    } else {
 #pragma unroll
-    for (int u = 0; u < MT; ++u)
-      if (u == tok)
+      for (int u = 0; u < MT; ++u)
+        if (u == tok)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) yacc[u][i] += part[i];
+          for (int i = 0; i < 8; ++i) yacc[u][i] += part[i];
+    }
   }
   __syncwarp();                                                 // scratch is rewritten by the next chunk
 }
@@ -492,12 +533,12 @@ __device__ __forceinline__ int q4_prep(const Q4Lane<KIND, MT>& L, uint32_t scrat
 
 // One chunk's arithmetic, its x prepared in `src` (the warp's scratch or a
 // cache slot) in the given mode (uniform over the warp).
-template <int KIND, int MT>
+template <int KIND, int MT, bool QTR = false>
 __device__ __forceinline__ void q4_math(const Q4Lane<KIND, MT>& L, uint32_t src, int lane, int m, int mode,
-                                        const XGroup (&G)[MT], float (&yacc)[MT][8]) {
-  if (mode == 3) q4_fixed<KIND, MT, 3>(L, src, lane, m, G, yacc);
-  else if (mode == 4) q4_fixed<KIND, MT, 4>(L, src, lane, m, G, yacc);
-  else q4_float<KIND, MT>(L, src, lane, m, yacc);
+                                        const XGroup (&G)[MT], float (&yacc)[MT][8], int h = 0) {
+  if (mode == 3) q4_fixed<KIND, MT, 3, QTR>(L, src, lane, m, G, yacc, h);
+  else if (mode == 4) q4_fixed<KIND, MT, 4, QTR>(L, src, lane, m, G, yacc, h);
+  else q4_float<KIND, MT, QTR>(L, src, lane, m, yacc, h);
 }
 
 // Q8: lane covers rows 8*qe + (0..7) of columns 8t + kc, t = 0..31.
@@ -632,12 +673,31 @@ __device__ __noinline__ void finish_segment(const GemvArgs& a, int64_t b, int w,
 
 // A stage's copies complete on its barrier: the chunk, plus `xbytes` of x
 // slices (0 when the CTA's x-slice cache serves the chunk).
-template <int KIND, int MT, class GemvArgs>
+// QTR: only quarter p.h of the chunk (its 8 rows' codes and scale fields),
+// each piece at its place in the stage.
+template <int KIND, int MT, bool QTR, class GemvArgs>
 __device__ __forceinline__ void issue_chunk(const GemvArgs& a, const Pos& p, uint32_t xbytes, uint8_t* dst,
                                             uint64_t* bar) {
   constexpr int CB = chunk_bytes_of(KIND);
-  mbar_arrive_expect_tx(bar, CB + xbytes);
-  bulk_g2s(dst, p.w, CB, bar);
+  if constexpr (QTR) {
+    const int h = p.h;
+    if constexpr (KIND == kQ4_1) {
+      mbar_arrive_expect_tx(bar, 1024 + 2 * 128 + xbytes);
+      bulk_g2s(dst + 1024 * h, p.w + 1024 * h, 1024, bar);                       // codes of rows 8h .. 8h+7
+      bulk_g2s(dst + kQ41Scale + 128 * h, p.w + kQ41Scale + 128 * h, 128, bar);  // their scales
+      bulk_g2s(dst + kQ41Zero + 128 * h, p.w + kQ41Zero + 128 * h, 128, bar);    // their zeros
+    } else {
+      mbar_arrive_expect_tx(bar, 1024 + 2 * 64 + 2 * 16 + xbytes);
+      bulk_g2s(dst + 1024 * h, p.w + 1024 * h, 1024, bar);
+      bulk_g2s(dst + kQ4KSc + 64 * h, p.w + kQ4KSc + 64 * h, 64, bar);
+      bulk_g2s(dst + kQ4KMn + 64 * h, p.w + kQ4KMn + 64 * h, 64, bar);
+      bulk_g2s(dst + kQ4KS + 16 * h, p.w + kQ4KS + 16 * h, 16, bar);
+      bulk_g2s(dst + kQ4KM + 16 * h, p.w + kQ4KM + 16 * h, 16, bar);
+    }
+  } else {
+    mbar_arrive_expect_tx(bar, CB + xbytes);
+    bulk_g2s(dst, p.w, CB, bar);
+  }
 }
 template <int KIND, int MT, class GemvArgs>
 __device__ __forceinline__ void issue_xslice(const GemvArgs& a, const Pos& p, int m, uint8_t* dst, uint64_t* bar) {
@@ -665,12 +725,16 @@ constexpr int gemv_max_threads() {
   return MT == 1 ? 512 : 256;
 }
 
-template <int KIND, int MAXB, int MT>
+// QTR: the index space counts quarters of chunks (a small launch spreads each
+// chunk's rows over four warps, so that one warp's arithmetic on one chunk is
+// not the launch's critical path).
+template <int KIND, int MAXB, int MT, bool QTR = false>
 __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = chunk_bytes_of(KIND);                         // a ring stage holds one chunk
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
-  constexpr bool XC = Q4 && MT == 1;                               // may use the x-slice cache
+  constexpr bool XC = Q4 && MT == 1 && !QTR;                       // may use the x-slice cache
+  static_assert(!QTR || (Q4 && MT == 1), "quarters: 4-bit kinds, one token");
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int m = (MT == 1) ? 1 : a.m;
@@ -694,7 +758,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   const int n = static_cast<int>(hi - lo);                     // chunks of this warp (>= 1)
 
   Pos cur{}, pre{};                         // chunk being processed / next chunk to fetch
-  cur.seek<CB>(a, lo);
+  cur.seek<CB, QTR>(a, lo);
   pre = cur;
   if (lane == 0) {
     for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
@@ -703,8 +767,8 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     // waiting on the previous grid; their x slices follow after the wait
     Pos p = pre;
     for (int s = 0; s < stages && s < n; ++s) {
-      issue_chunk<KIND, MT>(a, p, static_cast<uint32_t>(m * kXSliceBytes), ring + s * CB, &bars[s]);
-      p.next<CB>(a);
+      issue_chunk<KIND, MT, QTR>(a, p, static_cast<uint32_t>(m * kXSliceBytes), ring + s * CB, &bars[s]);
+      p.next<CB, QTR>(a);
     }
   }
   if (XC && a.xslots > 0 && threadIdx.x == 32 * (nwarps - 1)) {
@@ -712,8 +776,8 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     // used when they fit and each is reused four times on average (below
     // that, filling it costs the short launches more than it saves)
     Pos p0{}, p1{};
-    p0.seek<CB>(a, Lc);
-    p1.seek<CB>(a, Hc - 1);
+    p0.seek<CB, QTR>(a, Lc);
+    p1.seek<CB, QTR>(a, Hc - 1);
     int ok = p1.it - p0.it < kXTabItems, total = 0;
     for (int it = p0.it; ok && it <= p1.it; ++it) {
       const GemvItemDev& I = a.items[it];
@@ -737,7 +801,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   }
   if (threadIdx.x == blockDim.x - 1) {
     Pos e{};
-    e.seek<CB>(a, Hc - 1);
+    e.seek<CB, QTR>(a, Hc - 1);
     const int64_t r1 = a.items[e.it].cbase + (static_cast<int64_t>(e.tr) + 1) * a.items[e.it].TC;
     s_clast = r1 > Hc ? cta_of(r1 - 1, a.T, a.grid) : b;
   }
@@ -755,7 +819,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
   // serves them); every lane walks `pre`, so that it stays warp-uniform
   for (int s = 0; s < stages && s < n; ++s) {
     if (lane == 0) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
-    pre.next<CB>(a);
+    pre.next<CB, QTR>(a);
   }
   if (xc) {
     // fill the cache: warp w prepares slices w, w + nwarps, ...; each lane
@@ -822,7 +886,7 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     int mode = 0;
     uint32_t src = scratch;
     if constexpr (Q4) {
-      q4_read<KIND, MT>(st, xs, !xc, lane, m, q4l);
+      q4_read<KIND, MT, QTR>(st, xs, !xc, lane, m, q4l, cur.h);
       if (XC && xc) {
         src = xcache + xslot_of(cur) * kXSlotBytes;
         const uint32_t gr = src + kXSlotG + (lane & 7) * 32;
@@ -844,13 +908,13 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     __syncwarp();
     if (j + stages < n) {
       if (lane == 0) {
-        issue_chunk<KIND, MT>(a, pre, xbytes, ring + s * CB, &bars[s]);
+        issue_chunk<KIND, MT, QTR>(a, pre, xbytes, ring + s * CB, &bars[s]);
         if (!xc) issue_xslice<KIND, MT>(a, pre, m, xsl + s * MT * kXSliceBytes, &bars[s]);
       }
-      pre.next<CB>(a);
+      pre.next<CB, QTR>(a);
     }
-    if constexpr (Q4) q4_math<KIND, MT>(q4l, src, lane, m, mode, G, yacc);
-    cur.next<CB>(a);
+    if constexpr (Q4) q4_math<KIND, MT, QTR>(q4l, src, lane, m, mode, G, yacc, cur.h);
+    cur.next<CB, QTR>(a);
     if (++s == stages) s = 0;
   }
   if (failed) {
@@ -890,6 +954,9 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
 
 // Chunks per SM from which a 4-bit single-token launch runs two CTAs per SM.
 constexpr int kTwoCtaChunksPerSm = 128;
+// Chunks per SM up to which a 4-bit single-token launch takes quarters of
+// chunks as its units.
+constexpr int kQuarterChunksPerSm = 8;
 
 static int gemv_max_warps(int kind, int MT) {
   (void)kind;
@@ -908,6 +975,30 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
            static_cast<uint64_t>(w) * st * MT * kXSliceBytes;
   };
   auto need = [&](int w, int st) { return base(w, st) + static_cast<uint64_t>(w) * MT * kScratchBytes; };
+  p->quarter = 0;
+  if ((kind == kQ4_1 || kind == kQ4_K) && MT == 1 && T <= static_cast<int64_t>(kQuarterChunksPerSm) * info.sms) {
+    // A small one-token 4-bit launch (at most kQuarterChunksPerSm chunks per
+    // SM) is latency-bound: a warp's arithmetic on one chunk lies on its
+    // critical path.  Its units are quarters of chunks (8 rows each), up to
+    // 16 warps per CTA over CTAs of at least 4 chunks, one CTA per SM.
+    const uint64_t qcap = static_cast<uint64_t>(info.max_smem_optin) - 512;
+    int w = kMaxGemvWarps;
+    while (w > 1 && need(w, 2) > qcap) w /= 2;
+    if (need(w, 2) > qcap) return false;
+    int64_t grid = T / 4;
+    if (grid < 1) grid = 1;
+    if (grid > info.sms) grid = info.sms;
+    if (grid > kMaxCtas) grid = kMaxCtas;
+    const int64_t per_cta = 4 * T / grid;          // quarters per CTA; every warp gets at least one
+    if (per_cta < w) w = static_cast<int>(per_cta);
+    p->warps = w;
+    p->stages = 2;
+    p->grid = static_cast<int>(grid);
+    p->smem = need(w, 2);
+    p->xslots = 0;
+    p->quarter = 1;
+    return true;
+  }
   // Eight warps per CTA, each streaming a longer run of chunks, measured best
   // on GB300 against 12 and 16.  4-bit chunks: the CTA stays within half an
   // SM's shared memory, so that the next launch in the stream (programmatic
@@ -974,9 +1065,9 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int
   return kWsErrBytes + static_cast<uint64_t>(kMaxCtas) * MT * 32 * 8;
 }
 
-template <int KIND, int MAXB, int MT>
+template <int KIND, int MAXB, int MT, bool QTR = false>
 static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT>));
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT, QTR>));
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: SMs freed by the previous grid start this
   // one at once; the kernel waits for the previous grid before touching x, y
@@ -991,25 +1082,45 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB, MT>, a);
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB, MT, QTR>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+// The item table in units: chunks, or (unit = 4) quarters of chunks.
 template <int MAXB>
-static void fill_items(GemvArgsT<MAXB>& a, const GemvItem* items, int n) {
+static void fill_items(GemvArgsT<MAXB>& a, const GemvItem* items, int n, int unit = 1) {
   int64_t T = 0;
   for (int i = 0; i < n; ++i) {
     a.items[i].chunks = static_cast<const uint8_t*>(items[i].chunks);
     a.items[i].x = static_cast<const uint8_t*>(items[i].x);
     a.items[i].y = items[i].y;
     a.items[i].cbase = T;
-    a.items[i].nchunks = items[i].TR * items[i].TC;
-    a.items[i].TC = static_cast<int32_t>(items[i].TC);
-    T += items[i].TR * items[i].TC;
+    a.items[i].nchunks = items[i].TR * items[i].TC * unit;
+    a.items[i].TC = static_cast<int32_t>(items[i].TC * unit);
+    T += items[i].TR * items[i].TC * unit;
   }
   a.nitems = n;
   a.T = T;
+}
+
+// One-token launch of a planned GEMV (item table already in the plan's units).
+template <int MAXB>
+static cudaError_t launch_one_token(int kind, const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
+  if (p.quarter) {
+    switch (kind) {
+      case kQ4_1: return launch_gemv_t<kQ4_1, MAXB, 1, true>(a, p, s);
+      case kQ4_K: return launch_gemv_t<kQ4_K, MAXB, 1, true>(a, p, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (kind) {
+    case kQ4_1: return launch_gemv_t<kQ4_1, MAXB, 1>(a, p, s);
+    case kQ4_K: return launch_gemv_t<kQ4_K, MAXB, 1>(a, p, s);
+    case kQ8_KR: return launch_gemv_t<kQ8_KR, MAXB, 1>(a, p, s);
+    case kQ8_BLK: return launch_gemv_t<kQ8_BLK, MAXB, 1>(a, p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int MAXB>
@@ -1042,6 +1153,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   a.top1_row_base = top1 ? top1->row_base : 0u;
   GemvPlan p;
   if (!gemv_plan(kind, a.T, info, &p, 1)) return cudaErrorInvalidValue;
+  if (p.quarter) fill_items(a, items, n, 4);
   fill_workspace(a, workspace);
   a.grid = p.grid;
   a.stages = p.stages;
@@ -1054,13 +1166,7 @@ static cudaError_t launch_gemv_sized(int kind, const GemvItem* items, int n, int
   a.top1_idx = top1 ? top1->idx : nullptr;
   a.top1_key_out = top1 ? top1->key : nullptr;
   a.top1_row_base = top1 ? top1->row_base : 0u;
-  switch (kind) {
-    case kQ4_1: return launch_gemv_t<kQ4_1, MAXB, 1>(a, p, s);
-    case kQ4_K: return launch_gemv_t<kQ4_K, MAXB, 1>(a, p, s);
-    case kQ8_KR: return launch_gemv_t<kQ8_KR, MAXB, 1>(a, p, s);
-    case kQ8_BLK: return launch_gemv_t<kQ8_BLK, MAXB, 1>(a, p, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return launch_one_token<MAXB>(kind, a, p, s);
 }
 
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
@@ -1112,13 +1218,8 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
   a.top1_key_out = nullptr;
   a.top1_row_base = 0u;
   if (MT == 1) {                                  // one token: the single-GEMV kernel itself
-    switch (kind) {
-      case kQ4_1: return launch_gemv_t<kQ4_1, 1, 1>(a, p, s);
-      case kQ4_K: return launch_gemv_t<kQ4_K, 1, 1>(a, p, s);
-      case kQ8_KR: return launch_gemv_t<kQ8_KR, 1, 1>(a, p, s);
-      case kQ8_BLK: return launch_gemv_t<kQ8_BLK, 1, 1>(a, p, s);
-      default: return cudaErrorInvalidValue;
-    }
+    if (p.quarter) fill_items(a, &item, 1, 4);
+    return launch_one_token<1>(kind, a, p, s);
   }
   if (MT == 2) {
     switch (kind) {

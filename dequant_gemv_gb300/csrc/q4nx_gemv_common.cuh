@@ -176,19 +176,23 @@ __device__ __forceinline__ void q4_x_planes(const uint4 xr, int E, uint32_t scra
 }
 
 
-// Position of a chunk in the batch: item, tile row and column, with the
-// chunk's address and its x slice's, and the item's tile columns and chunks
-// left.  Workers walk their ranges in order, so a position advances by one
-// chunk with pointer increments; the item table (kernel parameters, read with
-// a dynamic index) is read only when the walk enters the next item.
+// Position of a unit in the batch: item, tile row and column, with the
+// chunk's address and its x slice's, and the item's tile columns and units
+// left.  A unit is a chunk, or with QTR a quarter of one (8 of its 32 rows,
+// quarter h): then the item table counts units (4 per chunk) and `tc` is the
+// unit column (chunk column tc / 4).  Workers walk their ranges in order, so a
+// position advances by one unit with pointer increments; the item table (kernel
+// parameters, read with a dynamic index) is read only when the walk enters the
+// next item.
 struct Pos {
   int it;
   int32_t tr, tc;
   int32_t TC;
-  int32_t left;                     // chunks of the item from this one to its end (tile counts fit 31 bits)
+  int32_t h;                        // quarter of the chunk (QTR), else 0
+  int32_t left;                     // units of the item from this one to its end (tile counts fit 31 bits)
   const uint8_t* w;                 // this chunk
   const uint8_t* x;                 // the x slice of its tile column (token 0)
-  template <int CB, class GemvArgs>
+  template <int CB, bool QTR, class GemvArgs>
   __device__ __forceinline__ void enter(const GemvArgs& a, int item, int64_t local) {
     const GemvItemDev& I = a.items[item];
     it = item;
@@ -196,29 +200,35 @@ struct Pos {
     left = static_cast<int32_t>(I.nchunks - local);
     tr = static_cast<int32_t>(local / TC);
     tc = static_cast<int32_t>(local - static_cast<int64_t>(tr) * TC);
-    w = I.chunks + local * CB;
-    x = I.x + static_cast<int64_t>(tc) * kXSliceBytes;
+    const int32_t cc = QTR ? tc >> 2 : tc;                      // chunk column
+    h = QTR ? tc & 3 : 0;
+    w = I.chunks + (static_cast<int64_t>(tr) * (QTR ? TC >> 2 : TC) + cc) * CB;
+    x = I.x + static_cast<int64_t>(cc) * kXSliceBytes;
   }
-  template <int CB, class GemvArgs>
+  template <int CB, bool QTR, class GemvArgs>
   __device__ __forceinline__ void seek(const GemvArgs& a, int64_t c) {
     int lo = 0, hi = a.nitems - 1;                  // last item with cbase <= c
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (a.items[mid].cbase <= c) lo = mid; else hi = mid - 1;
     }
-    enter<CB>(a, lo, c - a.items[lo].cbase);
+    enter<CB, QTR>(a, lo, c - a.items[lo].cbase);
   }
-  template <int CB, class GemvArgs>
+  template <int CB, bool QTR, class GemvArgs>
   __device__ __forceinline__ void next(const GemvArgs& a) {
-    w += CB;
-    x += kXSliceBytes;
-    if (++tc == TC) { tc = 0; ++tr; x -= static_cast<int64_t>(TC) * kXSliceBytes; }
-    if (--left == 0 && it + 1 < a.nitems) {                         // the next item's first chunk
+    if (!QTR || ++h == 4) {
+      h = 0;
+      w += CB;
+      x += kXSliceBytes;
+    }
+    if (++tc == TC) { tc = 0; ++tr; x -= static_cast<int64_t>(QTR ? TC >> 2 : TC) * kXSliceBytes; }
+    if (--left == 0 && it + 1 < a.nitems) {                         // the next item's first unit
       const GemvItemDev& I = a.items[++it];
       TC = I.TC;
       left = static_cast<int32_t>(I.nchunks);
       tr = 0;
       tc = 0;
+      h = 0;
       w = I.chunks;
       x = I.x;
     }

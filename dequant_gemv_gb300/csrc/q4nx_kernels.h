@@ -33,6 +33,7 @@ struct GemvPlan {
   int grid = 0;        // CTAs, each owning a contiguous range of chunks
   size_t smem = 0;     // dynamic shared memory bytes
   int xslots = 0;      // x-slice cache slots (4-bit kinds, one token)
+  int quarter = 0;     // the units are quarters of chunks (small 4-bit launches, one token)
 };
 bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan, int tokens);
 uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int tokens = 1);
