@@ -51,7 +51,8 @@
 // each wait or commit in that single issuing thread delays the tensor pipe.
 //
 // Work split (stream-K): the (tile, k-step) units are cut into one contiguous
-// range per CTA.  A tile shared by several CTAs is finished by the CTA that
+// range per CTA (for shapes whose tiles allow it, into equal parts of every
+// tile; see the launch).  A tile shared by several CTAs is finished by the CTA that
 // holds its first k-step.  That CTA reaches the tile at the end of its range,
 // while the others (which hold the tile's later k-steps at the start of their
 // ranges) post their fp32 partials early; the finisher gathers them into its
@@ -897,6 +898,20 @@ cudaError_t launch_gemm_kind(EncodeTiled enc, const DeviceInfo& info, const void
   // at least 4 k-steps per CTA where the work allows it, at most one CTA per SM
   int64_t grid = (a.units + 3) / 4;
   if (grid > info.sms) grid = info.sms;
+  // Where the tiles allow it, every tile in the same number s of equal parts
+  // (s dividing the tile's k-steps, at least 4 k-steps a part, the grid
+  // tiles * s filling at least 60 % of the SMs): no CTA's range then lies
+  // inside a single tile, so a tile's parts finish together and its finisher
+  // does not wait for a CTA that holds only its middle (which posts at its
+  // own end); the SMs left free take the next launch's first copies.
+  // Measured on GB300, back to back: 12288x4096 14.38 -> 13.86 us (96 CTAs of
+  // one whole tile), 4096x12288 16.07 -> 15.06 us (128 CTAs of a quarter tile).
+  {
+    int64_t parts = 0;
+    for (int64_t sp = 1; sp <= TC / 4 && tiles * sp <= info.sms; ++sp)
+      if (TC % sp == 0) parts = sp;
+    if (parts > 0 && tiles * parts * 10 >= 6 * static_cast<int64_t>(info.sms)) grid = tiles * parts;
+  }
   if (grid > 1024) grid = 1024;
   if (grid < 1) grid = 1;
   a.grid = static_cast<int>(grid);
