@@ -233,7 +233,7 @@ template <int KIND, int MT>
 struct Q4Lane {
   uint4 xr[MT];
   uint4 cw[8];
-  uint32_t f0[8], f1[8];           // q4_1: scale, zero bits; Q4_K: S bits | M bits << 16, sc | mn << 16
+  uint32_t f0[8], f1[8];           // q4_1: scale, zero bf16 bits; Q4_K: the binary32 bits of S*sc, M*mn
 };
 
 // QTR: only quarter h's rows 8h + qr and 8h + 4 + qr, into entries 0 and 1.
@@ -255,8 +255,13 @@ __device__ __forceinline__ void q4_read(uint32_t st, uint32_t xs, bool with_x, i
       L.f0[i] = lds_u16(st + kQ41Scale + (r * 8 + g) * 2);
       L.f1[i] = lds_u16(st + kQ41Zero + (r * 8 + g) * 2);
     } else {
-      L.f0[i] = lds_u16(st + kQ4KS + r * 2) | (lds_u16(st + kQ4KM + r * 2) << 16);
-      L.f1[i] = lds_u8(st + kQ4KSc + r * 8 + g) | (lds_u8(st + kQ4KMn + r * 8 + g) << 16);
+      // the row's scale S*sc and min M*mn as binary32 bits (exact products:
+      // 8 x 6 significant bits); sc, mn < 64 become binary32 through the bits
+      // of 2^23 + v, less 2^23
+      const float sc = __uint_as_float(0x4B000000u | lds_u8(st + kQ4KSc + r * 8 + g)) - 8388608.0f;
+      const float mn = __uint_as_float(0x4B000000u | lds_u8(st + kQ4KMn + r * 8 + g)) - 8388608.0f;
+      L.f0[i] = __float_as_uint(bf16_bits_to_f32(lds_u16(st + kQ4KS + r * 2)) * sc);
+      L.f1[i] = __float_as_uint(bf16_bits_to_f32(lds_u16(st + kQ4KM + r * 2)) * mn);
     }
   }
 }
@@ -267,12 +272,9 @@ __device__ __forceinline__ void q4_scale_zero(const Q4Lane<KIND, MT>& L, int i, 
   if constexpr (KIND == kQ4_1) {
     s = bf16_bits_to_f32(L.f0[i]);
     z = bf16_bits_to_f32(L.f1[i]);
-  } else {                                         // exact products: 8 x 6 significant bits
-    // sc, mn < 64 as binary32: the bits of 2^23 + v, less 2^23
-    const float sc = __uint_as_float(0x4B000000u | (L.f1[i] & 0xFFFFu)) - 8388608.0f;
-    const float mn = __uint_as_float(0x4B000000u | (L.f1[i] >> 16)) - 8388608.0f;
-    s = bf16_bits_to_f32(L.f0[i] & 0xFFFFu) * sc;
-    z = bf16_bits_to_f32(L.f0[i] >> 16) * mn;
+  } else {                                         // formed when the stage was read
+    s = __uint_as_float(L.f0[i]);
+    z = __uint_as_float(L.f1[i]);
   }
 }
 
