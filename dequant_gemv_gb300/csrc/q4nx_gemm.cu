@@ -548,6 +548,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit_elect(&sh->drain);                   // every MMA issued so far has completed
     mbar_wait_bounded(&sh->drain, 0, 100000000ull);
+  } else if (warp >= kWarpDequant0 && ntiles == 1) {
+    // ------------------------------------- dequant, twelve warps (one tile)
+    // A CTA that holds a single tile runs its epilogue only at its end, so
+    // the epilogue warps share the decode until then: k-step j's 8 tasks
+    // (TMEM lane quarter t & 3, half t >> 2 of the k-step) go to warps
+    // 4 + (8j + t) mod 12, each of the 12 warps taking two of every three
+    // k-steps, always on its own lane quarter (t & 3 == warp & 3).  A stage
+    // still receives 8 arrivals per k-step, and a warp waits only on the
+    // k-steps it works on, so every parity it waits for is the next one.
+    const int d = warp - kWarpDequant0;              // 0 .. 11
+    const int i = warp & 3;                          // tile row (= TMEM lane quarter)
+    const uint32_t t_lane = static_cast<uint32_t>(32 * i) << 16;
+    for (int j = 0; j < n; ++j) {
+      const int t = (d + 12 - (8 * j) % 12) % 12;
+      if (t >= 8) continue;                          // another warp's k-step
+      const int qh = t >> 2;
+      const int ws = j % kWStages, st = j % kStages;
+      const uint32_t wph = (j / kWStages) & 1, ph = (j / kStages) & 1;
+      if (!wait_bar_warp(sh, &sh->w_full[ws], wph, a.err)) break;
+      uint32_t out[64];
+      if constexpr (P::kQ8) {
+        dequant_half_q8<KIND>(smem_u32(smem + kWOff + ws * kWBytes + i * kQ8Bytes), lane, qh, out);
+      } else {
+        const uint32_t wst = smem_u32(smem + kWOff + ws * kWBytes);
+        dequant_half(wst + i * kCodes, wst + 4 * kCodes + i * kScales, lane, qh, out);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->w_empty[ws]);  // the stage's bytes are in registers
+      if (!wait_bar_warp(sh, &sh->empty[st], ph ^ 1u, a.err)) break;
+      tc_fence_after();
+      const uint32_t tdst = tmem + t_lane + kTmemA + static_cast<uint32_t>(st) * kAStageCols + static_cast<uint32_t>(qh * 64);
+      tmem_st32_async(tdst, out);
+      tmem_st32_async(tdst + 32, out + 32);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->full[st]);
+    }
   } else if (warp >= kWarpDequant0 && warp < kWarpEpi0) {
     // ----------------------------------------------------------- dequant
     // Software-pipelined: the TMEM stores of k-step j stay in flight while
@@ -605,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->full[pst]);
     }
-  } else if (warp >= kWarpEpi0) {
+  }
+  if (warp >= kWarpEpi0) {
     // ----------------------------------------------------------- epilogue
     // Only a CTA's last tile can be one it finishes (its first k-step here,
     // later ones in other CTAs); the last CTA holding part of it is worked out
