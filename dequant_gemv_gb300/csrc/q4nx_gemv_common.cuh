@@ -26,9 +26,9 @@ struct GemvItemDev {
   const uint8_t* chunks;
   const uint8_t* x;        // bf16 [K] (token m at x + m * x_stride)
   void* y;                 // [N] (token m at y + m * y_stride elements)
-  int64_t cbase;           // first chunk of this item in the batch index space
-  int64_t nchunks;         // TR * TC
-  int32_t TC;
+  int64_t cbase;           // first unit of this item in the batch index space
+  int64_t nchunks;         // its units: TR * TC chunks (times 4 when the units are quarters of chunks)
+  int32_t TC;              // units per tile row: tile columns (times 4 for quarters)
 };
 
 // Kernel parameters; MAXB batch slots (instantiated for 1, 8 and 256 items so
@@ -37,14 +37,14 @@ template <int MAXB>
 struct GemvArgsT {
   GemvItemDev items[MAXB];
   int nitems;
-  int grid;                // CTAs; CTA b owns chunks [T b / grid, T (b+1) / grid)
+  int grid;                // CTAs; CTA b owns units [T b / grid, T (b+1) / grid)
   int stages;
   int xslots;              // 4-bit kinds, one token: x-slice cache slots in shared memory (0: none)
   int out_f32;
   int m;                   // tokens (1 unless one item against several tokens)
   int64_t x_stride;        // bytes between tokens' x
   int64_t y_stride;        // elements between tokens' y
-  int64_t T;               // chunks in the batch
+  int64_t T;               // units in the batch (chunks, or quarters of chunks)
   uint32_t* err;
   uint64_t* posted;        // [grid][MT][32]: a CTA's sums of its first tile row when an earlier CTA finishes it
   // top-1 mode (one item): instead of storing y, keep the largest (fp32 value,
