@@ -308,6 +308,37 @@ def test_matvec_basis_vectors_give_columns(kind):
         assert np.array_equal(A, np.abs(W[:, k]))
 
 
+def test_matvec_non_finite_activations_follow_ieee():
+    """Closed forms for a non-finite activation (IEEE arithmetic, which the
+    products of the weight formulas inherit): with x = +Inf at one column and
+    zeros elsewhere, a row gives +Inf where its weight at that column is
+    positive, -Inf where it is negative and NaN (0 * Inf) where it is exactly
+    zero; a NaN activation gives NaN on every row."""
+    K = 256
+    inf, ninf, nan = 0x7F80, 0xFF80, 0x7FC0
+    # rows of three kinds at column 40: w > 0 (code 11, zero -1.5 at scale
+    # 0.25: 1.25), w < 0 (code 2: -1.0) and w = 0 (the Q4_0 mapping, code 8)
+    f = _q4_1_const(1, 11, 0.25, -1.5)
+    f.codes[0, 10:20, :] = 2
+    f.codes[0, 20:32, :] = 8
+    f.scale[0, 20:32, :] = _bf16(0.25)
+    f.zero[0, 20:32, :] = _bf16(-8 * 0.25)
+    w = synth.pack(f)
+    W = oracle.weights_f64(w, oracle.Q4_1, 32, K)
+    assert (W[:10, 40] == 1.25).all() and (W[10:20, 40] == -1.0).all() and (W[20:, 40] == 0).all()
+    for bits, sign in ((inf, 1.0), (ninf, -1.0)):
+        x = np.zeros(K, np.uint16)
+        x[40] = bits
+        y, _ = oracle.matmul(w, oracle.Q4_1, 32, K, x)
+        assert (y[:10] == sign * np.inf).all()
+        assert (y[10:20] == -sign * np.inf).all()
+        assert np.isnan(y[20:]).all()
+    x = synth.activations(synth.rng(31), 1, K)[0].copy()
+    x[7] = nan
+    y, _ = oracle.matmul(w, oracle.Q4_1, 32, K, x)
+    assert np.isnan(y).all()
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_matmul_matches_numpy_float64(kind):
     N, K, M = 96, 768, 3
