@@ -243,6 +243,31 @@ def test_gemv_batch_mixed_shapes(q, kind):
     q.q4nx_check(device=DEV)
 
 
+@pytest.mark.parametrize("kind", [synth.Q4_1, synth.Q4_K])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemv_batch_small_launches(q, kind, out):
+    """Batches small enough (at most 8 chunks per SM) that the launch takes
+    quarters of chunks as units: the {q, k, v} and {gate, up} phases of a
+    Qwen3-0.6B-shaped layer, and a mix of tiny weights whose quarters fall
+    across item boundaries at every offset; every row matches the oracle."""
+    batches = [[(2048, 1024), (1024, 1024), (1024, 1024)],
+               [(3072, 1024), (3072, 1024)],
+               [(32, 256), (96, 768), (64, 512), (160, 1280), (32, 2304), (256, 256)]]
+    for bi, shapes in enumerate(batches):
+        items, refs = [], []
+        for i, (N, K) in enumerate(shapes):
+            f, w = synth.make(kind, N, K, synth.rng(33, bi, i))
+            x = synth.activations(synth.rng(34, bi, i), 1, K)[0]
+            y = torch.empty(N, dtype=torch.float32 if out == "f32" else torch.bfloat16, device=DEV)
+            items.append((q.Weight(to_dev_bytes(w), kind, N, K), to_dev_bf16(x), y))
+            refs.append((w, x, N, K))
+        q.q4nx_gemv_batch(items, out_dtype=out)
+        for (W, xt, y), (w, x, N, K) in zip(items, refs):
+            Y64, A = oracle.matmul(w, kind, N, K, x)
+            assert_within(out_values(y), Y64, A, out == "bf16", f"small batch {bi} kind {kind} {N}x{K}")
+    q.q4nx_check(device=DEV)
+
+
 def test_gemv_batch_qwen3_layer_bf16(q):
     """A Qwen3-0.6B-shaped layer (7 projections) in one launch, bf16 outputs."""
     items, refs = [], []
