@@ -54,7 +54,7 @@ __shared__ long long s_clast;
 // across the main loop.
 __shared__ long long s_range[2];
 
-// x-slice cache (4-bit kinds, one token).  Every warp used to turn the x
+// x-slice cache (4-bit kinds).  Every warp used to turn the x
 // slice of each chunk it read into digit planes, although the chunks of one
 // tile column share the slice: with a CTA's range spanning several tile rows,
 // that preparation was repeated for every row (a fifth of the arithmetic).
@@ -63,8 +63,11 @@ __shared__ long long s_range[2];
 // after the wait on the previous grid, into a 1280-byte slot: regions A and B
 // (512 B each) as in a warp's scratch, or the raw bf16 slice when the slice
 // needs the binary32 path; then per group 32 B: q0, xq0..xq3 and the slice's
-// mode (3 or 4 digit planes, 5 for binary32).  Slots of one item are its
-// touched tile columns in order, starting from column tc0 and wrapping.
+// mode (3 or 4 digit planes, 5 for binary32).  With several tokens a slot
+// holds every token's 1024 bytes of planes (the token stride of a warp's
+// scratch) and then every token's 256 bytes of group records, all prepared
+// in one mode: the largest any token's group needs.  Slots of one item are
+// its touched tile columns in order, starting from column tc0 and wrapping.
 __shared__ int4 s_xtab[kXTabItems];        // per touched item: {first slot, tc0, slots, TC}
 __shared__ int s_xinfo[4];                 // cache used (0/1), first touched item, slots in use, items touched
 
@@ -347,7 +350,8 @@ __device__ __forceinline__ float2 q4_rows2(const uint32_t (&lo)[2][4], const uin
 }
 
 // The exact-integer path for one chunk: rows 4i + qr of group g, every token,
-// NP digit planes per token in `scratch` (token stride kScratchBytes).
+// NP digit planes per token in `scratch` (token stride kScratchBytes, in a
+// warp's scratch and in a slot of the x-slice cache alike).
 template <int KIND, int MT, int NP, bool QTR = false>
 __device__ __forceinline__ void q4_fixed(const Q4Lane<KIND, MT>& L, uint32_t scratch, int lane, int m,
                                          const XGroup (&G)[MT], float (&yacc)[MT][8], int h = 0) {
@@ -730,12 +734,15 @@ constexpr int gemv_max_threads() {
 // QTR: the index space counts quarters of chunks (a small launch spreads each
 // chunk's rows over four warps, so that one warp's arithmetic on one chunk is
 // not the launch's critical path).
-template <int KIND, int MAXB, int MT, bool QTR = false>
+// XCT: the x-slice cache's code is compiled in (always for one token; for
+// several, only into the launches planned to use it -- its branch alone costs
+// those that do not up to 15 %).
+template <int KIND, int MAXB, int MT, bool QTR = false, bool XCT = true>
 __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int CB = chunk_bytes_of(KIND);                         // a ring stage holds one chunk
   constexpr bool Q4 = (KIND == kQ4_1 || KIND == kQ4_K);
-  constexpr bool XC = Q4 && MT == 1 && !QTR;                       // may use the x-slice cache
+  constexpr bool XC = Q4 && !QTR && XCT;                           // may use the x-slice cache
   static_assert(!QTR || (Q4 && MT == 1), "quarters: 4-bit kinds, one token");
   asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -791,7 +798,12 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
       total += ns;
       ok = total <= a.xslots;
     }
-    s_xinfo[0] = ok && Hc - Lc >= 4 * static_cast<int64_t>(total);
+    // (reused at least 4 times for one token; more than twice for several,
+    // whose preparation per chunk costs several times more.  Measured on
+    // GB300: a reuse of exactly 2 -- Q4_K 9728x2560 against 2 tokens -- lost
+    // 4 % to the fill's barrier, 2.5 -- q4_1 12288x4096 -- gained 7 %)
+    s_xinfo[0] = ok && (MT == 1 ? Hc - Lc >= 4 * static_cast<int64_t>(total)
+                                : Hc - Lc > 2 * static_cast<int64_t>(total));
     s_xinfo[1] = p0.it;
     s_xinfo[2] = total;
     s_xinfo[3] = p1.it - p0.it + 1;
@@ -828,10 +840,11 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     // loads its 16 bytes of up to four slices before preparing any
     const int nsl = s_xinfo[2], it0 = s_xinfo[1], nti = s_xinfo[3];
     const int gp = lane & 7, tp = lane >> 3;
-    for (int s0 = warp; s0 < nsl; s0 += 4 * nwarps) {
-      uint4 xr[4];
+    constexpr int kU = MT == 1 ? 4 : 1;              // slices loaded before any is prepared
+    for (int s0 = warp; s0 < nsl; s0 += kU * nwarps) {
+      uint4 xr[kU][MT];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const int sl = s0 + u * nwarps;
         if (sl < nsl) {
           int k = 0;                                  // the touched item holding slot sl
@@ -839,13 +852,16 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
           const int4 e = s_xtab[k];
           int tc = e.y + (sl - e.x);
           if (tc >= e.w) tc -= e.w;
-          xr[u] = ld_cg_u4(a.items[it0 + k].x + static_cast<int64_t>(tc) * kXSliceBytes + gp * 64 + tp * 16);
+          const uint8_t* xs0 = a.items[it0 + k].x + static_cast<int64_t>(tc) * kXSliceBytes + gp * 64 + tp * 16;
+#pragma unroll
+          for (int tok = 0; tok < MT; ++tok)
+            if (MT == 1 || tok < m) xr[u][tok] = ld_cg_u4(xs0 + tok * a.x_stride);
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const int sl = s0 + u * nwarps;
-        if (sl < nsl) xslot_fill(xr[u], xcache + sl * kXSlotBytes, lane);
+        if (sl < nsl) xslot_fill<MT>(xr[u], xcache + sl * (MT * kXSlotBytes), m, lane);
       }
     }
     __syncthreads();
@@ -890,15 +906,19 @@ __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(c
     if constexpr (Q4) {
       q4_read<KIND, MT, QTR>(st, xs, !xc, lane, m, q4l, cur.h);
       if (XC && xc) {
-        src = xcache + xslot_of(cur) * kXSlotBytes;
-        const uint32_t gr = src + kXSlotG + (lane & 7) * 32;
-        const uint4 g0 = lds128(gr), g1 = lds128(gr + 16);
-        G[0].q0 = __uint_as_float(g0.x);
-        G[0].xq[0] = __uint_as_float(g0.y);
-        G[0].xq[1] = __uint_as_float(g0.z);
-        G[0].xq[2] = __uint_as_float(g0.w);
-        G[0].xq[3] = __uint_as_float(g1.x);
-        mode = static_cast<int>(g1.y);                          // the slice's mode: uniform
+        src = xcache + xslot_of(cur) * (MT * kXSlotBytes);
+#pragma unroll
+        for (int tok = 0; tok < MT; ++tok) {
+          if (MT > 1 && tok >= m) break;
+          const uint32_t gr = src + MT * kScratchBytes + tok * kXRecBytes + (lane & 7) * 32;
+          const uint4 g0 = lds128(gr), g1 = lds128(gr + 16);
+          G[tok].q0 = __uint_as_float(g0.x);
+          G[tok].xq[0] = __uint_as_float(g0.y);
+          G[tok].xq[1] = __uint_as_float(g0.z);
+          G[tok].xq[2] = __uint_as_float(g0.w);
+          G[tok].xq[3] = __uint_as_float(g1.x);
+          mode = static_cast<int>(g1.y);                        // the slice's mode: uniform over its tokens
+        }
       } else {
         mode = q4_prep<KIND, MT>(q4l, scratch, lane, m, G);
       }
@@ -966,11 +986,11 @@ static int gemv_max_warps(int kind, int MT) {
   return 8;
 }
 
-bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT) {
+bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT, int64_t tc) {
   const int CB = chunk_bytes_of(kind);
   if (CB == 0 || info.sms <= 0 || T <= 0 || MT < 1) return false;
   // ring, barriers, row slots, counters and the per-warp x slices; then the
-  // per-warp scratch, or (4-bit kinds, one token) the x-slice cache
+  // per-warp scratch, or (4-bit kinds) the x-slice cache
   auto base = [&](int w, int st) {
     return static_cast<uint64_t>(w) * st * CB + align16(static_cast<uint64_t>(w) * st * 8) +
            static_cast<uint64_t>(w) * MT * kSlotBytes + align16(static_cast<uint64_t>(w) * kCntBytes) +
@@ -1057,6 +1077,26 @@ bool gemv_plan(int kind, int64_t T, const DeviceInfo& info, GemvPlan* p, int MT)
     p->xslots = static_cast<int>(room < static_cast<uint64_t>(kMaxXSlots) ? room : kMaxXSlots);
     const uint64_t with_cache = base(warps, stages) + static_cast<uint64_t>(p->xslots) * kXSlotBytes;
     if (with_cache > p->smem) p->smem = with_cache;
+  } else if ((kind == kQ4_1 || kind == kQ4_K) && MT > 1 && tc > 0 && tc <= kMaxXSlots &&
+             (T + grid - 1) / grid > 2 * tc) {
+    // Several tokens (one weight of tc tile columns): a CTA of L chunks
+    // touches min(L, tc) slices and caches them when L > 2 tc (the kernel's
+    // own test).  Each slice takes MT slots' worth; the ring gives up its
+    // fourth stage when the tc slices would not fit beside it, since
+    // preparing every token's planes once per chunk costs more than the
+    // shallower ring.
+    const uint64_t per = static_cast<uint64_t>(MT) * kXSlotBytes;
+    auto slots = [&](int st) { return cap > base(warps, st) ? (cap - base(warps, st)) / per : uint64_t{0}; };
+    int st = stages;
+    if (st > 3 && slots(st) < static_cast<uint64_t>(tc)) --st;
+    if (slots(st) >= static_cast<uint64_t>(tc)) {
+      const uint64_t room = slots(st);
+      p->xslots = static_cast<int>(room < static_cast<uint64_t>(kMaxXSlots) ? room : kMaxXSlots);
+      p->stages = st;
+      p->smem = need(warps, st);
+      const uint64_t with_cache = base(warps, st) + static_cast<uint64_t>(p->xslots) * per;
+      if (with_cache > p->smem) p->smem = with_cache;
+    }
   }
   return true;
 }
@@ -1067,9 +1107,9 @@ uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int
   return kWsErrBytes + static_cast<uint64_t>(kMaxCtas) * MT * 32 * 8;
 }
 
-template <int KIND, int MAXB, int MT, bool QTR = false>
+template <int KIND, int MAXB, int MT, bool QTR = false, bool XCT = true>
 static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cudaStream_t s) {
-  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT, QTR>));
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<KIND, MAXB, MT, QTR, XCT>));
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: SMs freed by the previous grid start this
   // one at once; the kernel waits for the previous grid before touching x, y
@@ -1084,7 +1124,7 @@ static cudaError_t launch_gemv_t(const GemvArgsT<MAXB>& a, const GemvPlan& p, cu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB, MT, QTR>, a);
+  e = cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, MAXB, MT, QTR, XCT>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1205,7 +1245,7 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
   GemvArgsT<1> a;
   fill_items(a, &item, 1);
   GemvPlan p;
-  if (!gemv_plan(kind, a.T, info, &p, MT)) return cudaErrorInvalidValue;
+  if (!gemv_plan(kind, a.T, info, &p, MT, item.TC)) return cudaErrorInvalidValue;
   fill_workspace(a, workspace);
   a.err = err;
   a.grid = p.grid;
@@ -1223,16 +1263,17 @@ cudaError_t launch_gemv_tokens(int kind, const GemvItem& item, int M, int out_f3
     if (p.quarter) fill_items(a, &item, 1, 4);
     return launch_one_token<1>(kind, a, p, s);
   }
+  const bool xc = p.xslots > 0;
   if (MT == 2) {
     switch (kind) {
-      case kQ4_1: return launch_gemv_t<kQ4_1, 1, 2>(a, p, s);
-      case kQ4_K: return launch_gemv_t<kQ4_K, 1, 2>(a, p, s);
+      case kQ4_1: return xc ? launch_gemv_t<kQ4_1, 1, 2, false, true>(a, p, s) : launch_gemv_t<kQ4_1, 1, 2, false, false>(a, p, s);
+      case kQ4_K: return xc ? launch_gemv_t<kQ4_K, 1, 2, false, true>(a, p, s) : launch_gemv_t<kQ4_K, 1, 2, false, false>(a, p, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (kind) {
-    case kQ4_1: return launch_gemv_t<kQ4_1, 1, 4>(a, p, s);
-    case kQ4_K: return launch_gemv_t<kQ4_K, 1, 4>(a, p, s);
+    case kQ4_1: return xc ? launch_gemv_t<kQ4_1, 1, 4, false, true>(a, p, s) : launch_gemv_t<kQ4_1, 1, 4, false, false>(a, p, s);
+    case kQ4_K: return xc ? launch_gemv_t<kQ4_K, 1, 4, false, true>(a, p, s) : launch_gemv_t<kQ4_K, 1, 4, false, false>(a, p, s);
     default: return cudaErrorInvalidValue;
   }
 }

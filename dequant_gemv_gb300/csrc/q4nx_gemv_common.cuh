@@ -39,7 +39,7 @@ struct GemvArgsT {
   int nitems;
   int grid;                // CTAs; CTA b owns units [T b / grid, T (b+1) / grid)
   int stages;
-  int xslots;              // 4-bit kinds, one token: x-slice cache slots in shared memory (0: none)
+  int xslots;              // 4-bit kinds: x-slice cache slots in shared memory, each m tokens (0: none)
   int out_f32;
   int m;                   // tokens (1 unless one item against several tokens)
   int64_t x_stride;        // bytes between tokens' x
@@ -58,8 +58,8 @@ struct GemvArgsT {
 };
 
 
-constexpr int kXSlotBytes = 1280;
-constexpr int kXSlotG = 1024;              // per-group records within a slot
+constexpr int kXRecBytes = 256;            // per token: the 8 groups' records in an x-slice cache slot
+constexpr int kXSlotBytes = kScratchBytes + kXRecBytes;   // per token and slice
 constexpr int kXTabItems = 16;
 constexpr int kMaxXSlots = 32;
 
@@ -242,31 +242,44 @@ __device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
   return v;
 }
 
-// One x slice (its bf16 values in this prep lane's xr) into cache slot `sa`:
-// 3 or 4 digit planes (the most any of its groups needs), or the raw slice
-// for the binary32 path; the group records hold q0, xq0..xq3 and that mode.
-__device__ __forceinline__ void xslot_fill(const uint4 xr, uint32_t sa, int lane) {
+// One x slice of each of m tokens (their bf16 values in this prep lane's
+// xr[tok]) into the cache slot at sa: token tok's planes at
+// sa + tok * kScratchBytes, as 3 or 4 digit planes (the most any group of any
+// token needs, so that the chunk's arithmetic takes one mode for all tokens),
+// or the raw slices for the binary32 path; its group records, q0, xq0..xq3
+// and that mode, at sa + MT * kScratchBytes + tok * kXRecBytes.
+template <int MT>
+__device__ __forceinline__ void xslot_fill(const uint4 (&xr)[MT], uint32_t sa, int m, int lane) {
   const int gp = lane & 7, tp = lane >> 3;
-  int E;
-  const int need = __reduce_max_sync(0xffffffffu, q4_x_need(xr, E));
-  XGroup G = {};
-  if (need == 3) {
-    q4_x_planes<3>(xr, E, sa, lane, G);
-  } else if (need == 4) {
-    q4_x_planes<4>(xr, E, sa, lane, G);
-  } else {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sa + (tp * 8 + gp) * 16), "r"(xr.x), "r"(xr.y),
-                 "r"(xr.z), "r"(xr.w)
-                 : "memory");
-  }
-  if (tp == 0) {
-    const uint32_t gr = sa + kXSlotG + gp * 32;
-    asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(gr), "f"(G.q0), "f"(G.xq[0]), "f"(G.xq[1]),
-                 "f"(G.xq[2])
-                 : "memory");
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(gr + 16), "r"(__float_as_uint(G.xq[3])),
-                 "r"(static_cast<uint32_t>(need)), "r"(0u), "r"(0u)
-                 : "memory");
+  int E[MT];
+  int need = 3;
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok)
+    if (MT == 1 || tok < m) need = max(need, q4_x_need(xr[tok], E[tok]));
+  need = __reduce_max_sync(0xffffffffu, need);
+#pragma unroll
+  for (int tok = 0; tok < MT; ++tok) {
+    if (MT > 1 && tok >= m) break;
+    const uint32_t st = sa + tok * kScratchBytes;
+    XGroup G = {};
+    if (need == 3) {
+      q4_x_planes<3>(xr[tok], E[tok], st, lane, G);
+    } else if (need == 4) {
+      q4_x_planes<4>(xr[tok], E[tok], st, lane, G);
+    } else {
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + (tp * 8 + gp) * 16), "r"(xr[tok].x),
+                   "r"(xr[tok].y), "r"(xr[tok].z), "r"(xr[tok].w)
+                   : "memory");
+    }
+    if (tp == 0) {
+      const uint32_t gr = sa + MT * kScratchBytes + tok * kXRecBytes + gp * 32;
+      asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(gr), "f"(G.q0), "f"(G.xq[0]), "f"(G.xq[1]),
+                   "f"(G.xq[2])
+                   : "memory");
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(gr + 16), "r"(__float_as_uint(G.xq[3])),
+                   "r"(static_cast<uint32_t>(need)), "r"(0u), "r"(0u)
+                   : "memory");
+    }
   }
 }
 

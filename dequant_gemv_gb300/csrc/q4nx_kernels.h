@@ -32,10 +32,11 @@ struct GemvPlan {
   int stages = 0;      // ring stages per warp
   int grid = 0;        // CTAs, each owning a contiguous range of chunks
   size_t smem = 0;     // dynamic shared memory bytes
-  int xslots = 0;      // x-slice cache slots (4-bit kinds, one token)
+  int xslots = 0;      // x-slice cache slots, one per slice holding every token (4-bit kinds)
   int quarter = 0;     // the units are quarters of chunks (small 4-bit launches, one token)
 };
-bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan, int tokens);
+// tc: tile columns of the launch's one weight (several tokens), else 0
+bool gemv_plan(int kind, int64_t total_chunks, const DeviceInfo& info, GemvPlan* plan, int tokens, int64_t tc = 0);
 uint64_t gemv_workspace_bytes(int64_t total_tile_rows, int64_t total_chunks, int tokens = 1);
 cudaError_t launch_gemv_batch(int kind, const GemvItem* items, int n, int out_f32, void* workspace,
                               const DeviceInfo& info, cudaStream_t s);

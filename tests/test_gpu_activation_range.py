@@ -18,6 +18,8 @@ Cases:
   * groups whose magnitudes span exactly 2^14 and just beyond;
   * every weight an exact zero: the output is exactly zero;
   * scales near 2^+-100;
+  * several tokens whose x slices, prepared once per CTA for all of them,
+    need different numbers of digit planes (the few-token x-slice cache);
   * one +Inf, -Inf or NaN activation (GEMV of every kind, the batched layer
     on the x-slice cache path, the tensor-core GEMM): each row meets the
     special value exactly as the binary64 sum does (0 * Inf = NaN).
@@ -226,6 +228,39 @@ def test_few_tokens_dynamic_range(q, kind, M, N, K):
     got = out_values(q.q4nx_gemm_m64(W2, to_dev_bf16(X), out_dtype="bf16"))
     Y64, A = oracle.matmul(w2, kind, N, K, X)
     assert_within(got, Y64, A, True, f"tokens kind {kind} M={M} {N}x{K} (random weights)")
+
+
+@pytest.mark.parametrize("kind,M", [(synth.Q4_1, 2), (synth.Q4_K, 2), (synth.Q4_K, 3), (synth.Q4_K, 4)])
+@pytest.mark.parametrize("N,K", [(16384, 1024), (12288, 4096)])
+@pytest.mark.parametrize("order", ["as_built", "reversed"])
+def test_few_tokens_cached_x_slices(q, kind, M, N, K, order):
+    """Shapes whose CTAs read each touched x slice more than twice (16384 x
+    1024: about 13 chunks per CTA over 4 slices; 12288 x 4096: about 40 over
+    16), so that the few-token kernel prepares every slice once for all
+    tokens, in the largest number of digit planes any token's group needs
+    (Q4_K at 3-4 tokens on 12288 x 4096 excepted: 16 slices of 4 tokens do
+    not fit beside its ring, and it prepares x per chunk).  The tokens mix
+    N(0, 1), outlier channels, the worked case and log-uniform magnitudes
+    (which need the binary32 path), in either order."""
+    f, w = q4_0_mapped_weight(kind, N, K, seed=M)
+    X = token_block(K, 4)
+    X = np.stack([X[3], X[1], X[0], X[2]])[:M]         # N(0, 1) first: its slices share a wider token's mode
+    if order == "reversed":
+        X = X[::-1].copy()
+    rows = None if N * K <= 20_000_000 else np.unique(np.concatenate([
+        np.arange(0, 128), np.arange(N - 128, N), np.random.default_rng(M).integers(0, N, 384)]))
+    W = q.Weight(to_dev_bytes(w), kind, N, K)
+    for out in ("f32", "bf16"):
+        got = out_values(q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype=out))
+        Y64, A = oracle.matmul(w, kind, N, K, X, rows=rows)
+        assert_within(got if rows is None else got[:, rows], Y64, A, out == "bf16",
+                      f"cached tokens kind {kind} M={M} {N}x{K} {order} {out}")
+    f2, w2 = synth.make(kind, N, K, synth.rng(53, kind, M))
+    W2 = q.Weight(to_dev_bytes(w2), kind, N, K)
+    got = out_values(q.q4nx_gemm_m64(W2, to_dev_bf16(X), out_dtype="f32"))
+    Y64, A = oracle.matmul(w2, kind, N, K, X, rows=rows)
+    assert_within(got if rows is None else got[:, rows], Y64, A, False,
+                  f"cached tokens kind {kind} M={M} {N}x{K} {order} (random weights)")
 
 
 @pytest.mark.parametrize("N,K", [(12288, 4096), (4096, 12288)])
