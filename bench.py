@@ -15,7 +15,9 @@ value      = weight GB/s of the whole job (chunk bytes / s), inputs resident in 
              (CUDA-graph replays of the step), max over ranks.
 e2e        = the same metric through the public API with host buffers: per step
              the activations go host->device from pinned memory, the step runs,
-             the outputs come back device->host, and the host synchronises.
+             the outputs come back device->host (copies on a second stream,
+             double-buffered, overlapping the neighbouring steps' launches),
+             and the host waits for each step's outputs, one step behind.
 roofline   = the dominant kernel (q4nx GEMV): algorithmic bytes per launch
              (chunks + x + y) / mean launch duration, against the measured HBM
              copy bandwidth.
@@ -271,6 +273,13 @@ def run_gpu(args, rank: int, world: int):
         return g
 
     graph = capture(step_batch)                 # one step (used for the end-to-end leg)
+    # the end-to-end leg's second set of device x / y buffers (double buffering)
+    xdev2 = torch.empty_like(xdev)
+    ydev2 = torch.empty_like(ydev)
+    y_host2 = torch.empty(ytot, dtype=torch.bfloat16, pin_memory=True)
+    step_batch2 = q.GemvBatch([(weights[i], xdev2[xoffs[i]:xoffs[i] + K], ydev2[yoffs[i]:yoffs[i] + N])
+                               for i, (_, _, N, K) in enumerate(mats)], "bf16", ws)
+    graph2 = capture(step_batch2)
     # the timed loop replays graphs of several consecutive steps, so that each
     # step's launch overlaps the previous one (programmatic dependent launch)
     # as in a decode loop; a step is still one launch over all 196 matrices
@@ -362,22 +371,47 @@ def run_gpu(args, rank: int, world: int):
     peak, peak_kind = _peaks()
     traffic = _traffic_if_current()
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers.  Every step copies
+    # its activations host -> device from pinned memory and reads its outputs
+    # back device -> host, each on a stream of its own and double-buffered, so
+    # that step i+1's input copy and step i's output read overlap the GEMV
+    # launches on the compute stream; the host waits for each step's outputs
+    # one step behind, and for the last step's before the clock stops.
     e2e_steps = max(3, min(args.steps, 200))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            xdev.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(ydev, non_blocking=True)
-            stream.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            xdev.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(ydev, non_blocking=True)
-            stream.synchronize()
-        t_e2e = time.perf_counter() - t0
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = ((xdev, ydev, y_host, graph), (xdev2, ydev2, y_host2, graph2))
+
+    def e2e_run(n):
+        x_ready = [torch.cuda.Event() for _ in range(2)]
+        k_done = [torch.cuda.Event() for _ in range(2)]
+        y_read = [None, None]
+        for i in range(n):
+            b = i % 2
+            xd, yd, yh, g = bufs[b]
+            with torch.cuda.stream(h2d_stream):
+                if i >= 2:
+                    h2d_stream.wait_event(k_done[b])           # step i-2 has read this x buffer
+                xd.copy_(x_host, non_blocking=True)
+                x_ready[b].record(h2d_stream)
+            with torch.cuda.stream(stream):
+                stream.wait_event(x_ready[b])
+                g.replay()                                     # (yd's step i-2 outputs reached the host first)
+                k_done[b].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(k_done[b])
+                yh.copy_(yd, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(d2h_stream)
+                y_read[b] = ev
+            if i >= 1:
+                y_read[1 - b].synchronize()                    # step i-1's outputs are on the host
+        y_read[(n - 1) % 2].synchronize()
+
+    e2e_run(4)
+    barrier()
+    t0 = time.perf_counter()
+    e2e_run(e2e_steps)
+    t_e2e = time.perf_counter() - t0
     t_e2e = max_over_ranks(t_e2e, world, dev)
     e2e_value = job_throughput(world, wtot, e2e_steps, t_e2e)
 
