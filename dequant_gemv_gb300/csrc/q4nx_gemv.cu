@@ -736,7 +736,7 @@ constexpr int gemv_max_threads() {
 // not the launch's critical path).
 // XCT: the x-slice cache's code is compiled in (always for one token; for
 // several, only into the launches planned to use it -- its branch alone costs
-// those that do not up to 15 %).
+// those that do not up to 17 %).
 template <int KIND, int MAXB, int MT, bool QTR = false, bool XCT = true>
 __global__ void __launch_bounds__(gemv_max_threads<KIND, MT>(), 1) gemv_kernel(const __grid_constant__ GemvArgsT<MAXB> a) {
   extern __shared__ __align__(128) uint8_t smem[];
