@@ -261,6 +261,19 @@ def run_gpu(args, rank: int, world: int):
             base = 7 * l
             for grp in ((0, 1, 2), (3,), (4, 5), (6,)):
                 per_layer.append(q.GemvBatch([items[base + j] for j in grp], "bf16", ws))
+        # the same schedule with the matrices that read the same activations
+        # stored as one weight (q|k|v and gate|up: adjacent chunk arrays, same
+        # K), so that each phase is one matrix on one x; k, v and up then read
+        # q's and gate's activations, as in a real layer
+        per_layer_merged = []
+        for l in range(synth.QWEN3_06B_LAYERS):
+            base = 7 * l
+            for grp in ((0, 1, 2), (3,), (4, 5), (6,)):
+                i0, i1 = base + grp[0], base + grp[-1]
+                N = sum(mats[base + j][2] for j in grp)
+                K = mats[i0][3]
+                Wm = q.Weight(wdev[offs[i0]:offs[i1] + (mats[i1][2] // 32) * (K // 256) * CHUNK], q.Q4NX_Q4_1, N, K)
+                per_layer_merged.append(q.GemvBatch([(Wm, xs[i0], ydev[yoffs[i0]:yoffs[i0] + N])], "bf16", ws))
     torch.cuda.synchronize()
 
     def capture(fn):
@@ -360,6 +373,10 @@ def run_gpu(args, rank: int, world: int):
         t_layer_ms = time_graph(g_layer, 200)
         alt["per_layer_4_launches_gbs"] = wtot / (t_layer_ms / 1e3) / 1e9
         alt["us_per_layer_dependent"] = t_layer_ms * 1e3 / synth.QWEN3_06B_LAYERS
+        g_merged = capture(lambda: [b() for b in per_layer_merged])
+        t_merged_ms = time_graph(g_merged, 200)
+        alt["us_per_layer_dependent_merged_qkv_gate_up"] = t_merged_ms * 1e3 / synth.QWEN3_06B_LAYERS
+        del g_merged
         g_single = capture(lambda: [q.q4nx_gemv(weights[i], xs[i], out=ys[i], ws=ws) for i in range(len(mats))])
         alt["one_launch_per_matrix_gbs"] = wtot / (time_graph(g_single, 100) / 1e3) / 1e9
         del g_layer, g_single

@@ -68,3 +68,35 @@ def test_max_batch_items(q):
         assert_within(out_values(y), Y64, A, False, f"item {i} {n}x{k}")
     with pytest.raises(ValueError):                     # one item past the maximum: refused before any launch
         q.q4nx_gemv_batch(items + items[:1], out_dtype="f32")
+
+
+def test_layer_phases_on_merged_weights(q):
+    """A decode layer's projections that read the same activations as one
+    weight each: q|k|v (2048 + 1024 + 1024 rows of 1024 columns, parts of
+    different heights) and gate|up (2 x 3072 rows), their chunk arrays
+    concatenated; o and down as they are.  The four phases run as one
+    q4nx_gemv_batch each, in order, every phase on one x; each part's rows are
+    checked against the oracle of its own weight, around every seam."""
+    layer = 3
+    parts = {mi: synth.workload_weight(WORKLOAD_ID, mi, layer=layer, shape=(n, k))[1]
+             for mi, (_, n, k) in enumerate(synth.QWEN3_06B_LAYER)}
+    shapes = [(n, k) for (_, n, k) in synth.QWEN3_06B_LAYER]
+    phases = [(0, 1, 2), (3,), (4, 5), (6,)]
+    rng = np.random.default_rng(17)
+    for p, grp in enumerate(phases):
+        K = shapes[grp[0]][1]
+        assert all(shapes[mi][1] == K for mi in grp)
+        N = sum(shapes[mi][0] for mi in grp)
+        x = synth.activations(synth.rng(62, layer, p), 1, K)[0]
+        W = q.Weight(to_dev_bytes(np.concatenate([parts[mi] for mi in grp])), synth.Q4_1, N, K)
+        y = torch.empty(N, dtype=torch.bfloat16, device=DEV)
+        q.q4nx_gemv_batch([(W, to_dev_bf16(x), y)], out_dtype="bf16")
+        got = out_values(y)
+        base = 0
+        for mi in grp:
+            n = shapes[mi][0]
+            rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(n - 40, n), rng.integers(0, n, 64)]))
+            Y64, A = oracle.matmul(parts[mi], synth.Q4_1, n, K, x, rows=rows)
+            assert_within(got[base + rows], Y64, A, True, f"phase {p} part {mi} ({n}x{K} at row {base})")
+            base += n
+    q.q4nx_check(device=DEV)
