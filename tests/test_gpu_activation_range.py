@@ -231,7 +231,7 @@ def test_few_tokens_dynamic_range(q, kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind,M", [(synth.Q4_1, 2), (synth.Q4_K, 2), (synth.Q4_K, 3), (synth.Q4_K, 4)])
-@pytest.mark.parametrize("N,K", [(16384, 1024), (12288, 4096)])
+@pytest.mark.parametrize("N,K", [(16384, 1024), (12288, 4096), (10240, 1024)])
 @pytest.mark.parametrize("order", ["as_built", "reversed"])
 def test_few_tokens_cached_x_slices(q, kind, M, N, K, order):
     """Shapes whose CTAs read each touched x slice more than twice (16384 x
@@ -239,7 +239,9 @@ def test_few_tokens_cached_x_slices(q, kind, M, N, K, order):
     16), so that the few-token kernel prepares every slice once for all
     tokens, in the largest number of digit planes any token's group needs
     (Q4_K at 3-4 tokens on 12288 x 4096 excepted: 16 slices of 4 tokens do
-    not fit beside its ring, and it prepares x per chunk).  The tokens mix
+    not fit beside its ring, and it prepares x per chunk).  10240 x 1024
+    mixes both in one launch: CTAs of 9 chunks over 4 slices use the cache,
+    those of 8 prepare x per chunk.  The tokens mix
     N(0, 1), outlier channels, the worked case and log-uniform magnitudes
     (which need the binary32 path), in either order."""
     f, w = q4_0_mapped_weight(kind, N, K, seed=M)
