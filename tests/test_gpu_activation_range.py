@@ -19,7 +19,8 @@ Cases:
   * every weight an exact zero: the output is exactly zero;
   * scales near 2^+-100;
   * several tokens whose x slices, prepared once per CTA for all of them,
-    need different numbers of digit planes (the few-token x-slice cache);
+    need different numbers of digit planes (the few-token x-slice cache),
+    also beside a token holding +Inf or NaN and an all-zero token;
   * one +Inf, -Inf or NaN activation (GEMV of every kind, the batched layer
     on the x-slice cache path, the tensor-core GEMM): each row meets the
     special value exactly as the binary64 sum does (0 * Inf = NaN).
@@ -390,6 +391,38 @@ def test_decode_layer_batch_with_inf_and_nan(q):
             assert_same_specials(out_values(y), Y64, f"layer matrix {mi}")
         else:
             assert_within(out_values(y), Y64, A, False, f"layer matrix {mi} beside special values")
+
+
+@pytest.mark.parametrize("kind,M", [(synth.Q4_1, 2), (synth.Q4_K, 2), (synth.Q4_K, 3), (synth.Q4_K, 4)])
+def test_few_tokens_cached_slices_with_special_values(q, kind, M):
+    """The few-token kernel with its x-slice cache (16384 x 1024: each CTA
+    reads its 4 slices about three times) when token 0 holds a +Inf, at four
+    tokens token 1 a NaN, and from three tokens the last is all zeros: a slice
+    holding a special value is prepared for every token on the binary32 path.
+    The special tokens' rows meet it as in binary64, the zero token's rows are
+    exactly 0 and the N(0, 1) token stays within the bar."""
+    N, K = 16384, 1024
+    f, w = synth.make(kind, N, K, synth.rng(54, kind, M))
+    X = synth.activations(synth.rng(54, 1, M), M, K).copy()
+    X[0, 700] = 0x7F80                                  # +Inf (slice 2)
+    specials = [0]
+    if M == 4:
+        X[1, 5] = 0x7FC0                                # NaN (slice 0)
+        specials.append(1)
+    zero = M - 1 if M >= 3 else None
+    if zero is not None:
+        X[zero, :] = 0
+    finite = [m for m in range(M) if m not in specials and m != zero]
+    assert len(finite) == 1
+    W = q.Weight(to_dev_bytes(w), kind, N, K)
+    got = out_values(q.q4nx_gemm_m64(W, to_dev_bf16(X), out_dtype="f32"))
+    Y64, A = oracle.matmul(w, kind, N, K, X)
+    for m in specials:
+        assert_same_specials(got[m], Y64[m], f"kind {kind} M={M} token {m}")
+    if zero is not None:
+        assert np.all(got[zero] == 0.0), "the all-zero token's rows"
+    m = finite[0]
+    assert_within(got[m], Y64[m], A[m], False, f"kind {kind} M={M} token {m} beside special values")
 
 
 def test_gemm_64_tokens_with_inf_and_nan(q):
